@@ -1,0 +1,49 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check that
+the pin suite rejects every one of them. The real oracle is never modified."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(os.path.dirname(HERE), "oracle", "alibi_oracle.c")
+
+# (name, exact source text, replacement)
+MUTANTS = [
+    ("bias_sign", "double B = -m * D;", "double B = m * D;"),
+    ("no_scale", "return s / sqrt((double)d);", "return s;"),
+    ("scale_by_d", "return s / sqrt((double)d);", "return s / (double)d;"),
+    ("q_dot_q", "content_score(qi, c->k + base + (size_t)j * c->d, c->d);\n        if (c->variant",
+     "content_score(qi, c->q + base + (size_t)j * c->d, c->d);\n        if (c->variant"),
+    ("mask_diagonal", "if (causal && j > i) return -INFINITY;", "if (causal && j >= i) return -INFINITY;"),
+    ("value_row_i", "const float *vj = c->v + base + (size_t)j * c->d;",
+     "const float *vj = c->v + base + (size_t)i * c->d;"),
+    ("slope_exponent_h", "*num = 8 * (h + 1);", "*num = 8 * h + 4;"),
+    ("appended_odd_entries", "*num = 8 * (2 * t + 1);", "*num = 8 * (2 * t + 2);"),
+    ("lse_without_max", "if (c->lse) c->lse[r] = M + log(Z);", "if (c->lse) c->lse[r] = log(Z);"),
+    ("decode_position", "const long pos = (long)c->L - 1;", "const long pos = (long)c->L;"),
+    ("underflow_no_max", "double e = x[j] - M;", "double e = x[j];"),
+    ("threshold_127", "t[2] = -126.0 * ln2;", "t[2] = -127.0 * ln2;"),
+    ("softcap_no_z", "return z * tanh(a / z);", "return tanh(a / z);"),
+    ("logdist_no_plus1", "D = log(D + 1.0);", "D = log(D);"),
+    ("clamp_min", "if ((variant & ORACLE_CLAMP) && B < c_clamp) B = c_clamp;",
+     "if ((variant & ORACLE_CLAMP) && B > c_clamp) B = c_clamp;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mut_c = tmp_path / f"{name}.c"
+    mut_c.write_text(src.replace(old, new))
+    mut_so = tmp_path / f"{name}.so"
+    oracle.compile_to(str(mut_c), str(mut_so))
+    env = dict(os.environ, ALIBI_ORACLE_LIB=str(mut_so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(HERE, "test_oracle_pins.py")],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
