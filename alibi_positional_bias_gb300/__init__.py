@@ -1,0 +1,224 @@
+"""GB300-native ALiBi causal attention: Python binding of the C ABI (include/alibi.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``_build/libalibi_gb300.so``. There is no CPU fallback; if the library
+is missing or fails to load, every call raises.
+
+The functions carry the names of the C entry points. Tensors are torch CUDA
+tensors (torch supplies device memory and streams); ``stream`` defaults to
+torch's current stream on the tensors' device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import _build
+
+__all__ = [
+    "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
+    "alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
+    "alibi_attn_underflow_bf16", "alibi_check_error",
+]
+
+ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AlibiError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {alibi_status_str(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load the CUDA library (optionally building it first). Raises if it cannot be loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing and not os.path.exists(path):
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"ALiBi CUDA library not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        vp, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.alibi_version.restype = I
+        lib.alibi_status_str.argtypes = [I]
+        lib.alibi_status_str.restype = ctypes.c_char_p
+        lib.alibi_slopes.argtypes = [I, ctypes.POINTER(F)]
+        lib.alibi_attn_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
+        lib.alibi_attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
+        lib.alibi_attn_decode.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
+        lib.alibi_attn_probs_f32.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
+        lib.alibi_attn_decode_splits.argtypes = [I, I, I, I]
+        lib.alibi_attn_underflow_bf16.argtypes = [vp, vp, I, I, I, I, F, vp, vp]
+        lib.alibi_check_error.argtypes = [vp]
+        for name in ("alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits",
+                     "alibi_attn_probs_f32",
+                     "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_slopes"):
+            getattr(lib, name).restype = I
+        _lib = lib
+        return lib
+
+
+def exported_symbols(names) -> dict:
+    """Which of ``names`` the loaded library exports (no device work)."""
+    lib = load()
+    return {n: hasattr(lib, n) for n in names}
+
+
+def _check(status: int, where: str):
+    if status != ALIBI_OK:
+        raise AlibiError(status, where)
+
+
+def _stream(stream, device):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, dtype, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# --------------------------------------------------------------------- entry points
+
+def alibi_version() -> int:
+    return load().alibi_version()
+
+
+def alibi_status_str(status: int) -> str:
+    try:
+        return load().alibi_status_str(int(status)).decode()
+    except Exception:  # library unavailable while formatting an error
+        return f"status {status}"
+
+
+def alibi_slopes(H: int) -> np.ndarray:
+    """fp32 ALiBi slopes for H heads (host computation in the library)."""
+    out = np.empty(H, dtype=np.float32)
+    _check(load().alibi_slopes(int(H), out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), "alibi_slopes")
+    return out
+
+
+def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None, want_lse: bool = True):
+    """bf16 causal prefill on the tensor cores. q, k, v: [B, H, N, d] bf16 CUDA tensors."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.bfloat16, q.shape, "k")
+    _need(v, torch.bfloat16, q.shape, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, q.shape, "out")
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, (B, H, N), "lse")
+    _check(load().alibi_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                 _stream(stream, q.device)), "alibi_attn_fwd")
+    return out, lse
+
+
+def alibi_attn_fwd_f32(q, k, v, out=None, lse=None, causal: bool = True, stream=None):
+    """fp32 causal prefill (reference precision). q, k, v: [B, H, N, d] fp32 CUDA tensors."""
+    import torch
+    _need(q, torch.float32, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.float32, q.shape, "k")
+    _need(v, torch.float32, q.shape, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, q.shape, "out")
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _need(lse, torch.float32, (B, H, N), "lse")
+    _check(load().alibi_attn_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                     int(bool(causal)), _stream(stream, q.device)), "alibi_attn_fwd_f32")
+    return out, lse
+
+
+def alibi_attn_decode(q, kcache, vcache, out=None, stream=None):
+    """bf16 decode: q [B, H, d] at position L-1 against caches [B, H, L, d]."""
+    import torch
+    _need(kcache, torch.bfloat16, None, "kcache")
+    B, H, L, d = kcache.shape
+    _need(vcache, torch.bfloat16, kcache.shape, "vcache")
+    _need(q, torch.bfloat16, (B, H, d), "q")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, (B, H, d), "out")
+    _check(load().alibi_attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, L, d,
+                                    _stream(stream, q.device)), "alibi_attn_decode")
+    return out
+
+
+def alibi_attn_decode_splits(B: int, H: int, L: int, d: int) -> int:
+    """KV splits alibi_attn_decode uses for this shape (1 = single kernel, no partials)."""
+    s = load().alibi_attn_decode_splits(int(B), int(H), int(L), int(d))
+    if s < 0:
+        raise AlibiError(s, "alibi_attn_decode_splits")
+    return s
+
+
+def alibi_attn_probs_f32(q, k, lse, P=None, stream=None):
+    """fp32 attention weights [B, H, N, N] from the LSE of alibi_attn_fwd_f32."""
+    import torch
+    _need(q, torch.float32, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.float32, q.shape, "k")
+    _need(lse, torch.float32, (B, H, N), "lse")
+    if P is None:
+        P = torch.empty((B, H, N, N), dtype=torch.float32, device=q.device)
+    _need(P, torch.float32, (B, H, N, N), "P")
+    _check(load().alibi_attn_probs_f32(_ptr(q), _ptr(k), _ptr(lse), _ptr(P), B, H, N, d,
+                                       _stream(stream, q.device)), "alibi_attn_probs_f32")
+    return P
+
+
+def alibi_attn_underflow_bf16(q, k, tau: float, counts=None, stream=None):
+    """Per-head counts of causal pairs whose max-subtracted exponent is <= tau."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.bfloat16, q.shape, "k")
+    if counts is None:
+        counts = torch.empty((H,), dtype=torch.int64, device=q.device)
+    _need(counts, torch.int64, (H,), "counts")
+    _check(load().alibi_attn_underflow_bf16(_ptr(q), _ptr(k), B, H, N, d, ctypes.c_float(tau), _ptr(counts),
+                                            _stream(stream, q.device)), "alibi_attn_underflow_bf16")
+    return counts
+
+
+def alibi_check_error(stream=None, device=None) -> None:
+    """Synchronise and raise if a kernel recorded a device-side failure."""
+    _check(load().alibi_check_error(_stream(stream, device)), "alibi_check_error")

@@ -1,0 +1,277 @@
+// ALiBi decode: one new query per (b, h) against a bf16 KV cache of L positions.
+//
+// The query sits at its true sequence position L - 1 ("ALiBi: Attention with
+// Linear Biases" (abhik.ai), the KV-cache paragraph after the full-sequence
+// example), so key j has bias -m_h (L - 1 - j):
+//   s_j = q.k_j / sqrt(d) - m_h (L - 1 - j),  out = sum_j softmax_j(s) v_j
+// with the max-shifted softmax of "When Attention Goes Blind" (arXiv
+// 2608.03994), App. B.1, evaluated online and merged across splits.
+//
+// Memory-bound design: the cache is streamed once with 16-byte non-caching
+// loads. A half-warp owns one key row (16 lanes x 8 bf16 = 256 bytes = d 128),
+// so a warp-wide load covers two adjacent rows (512 contiguous bytes). Each
+// warp issues 16 K and 16 V loads (8 keys per half-warp) before using any of
+// them, keeping ~8 KB per warp in flight. Grid = (splits, B*H); each CTA (8
+// warps) streams a contiguous slice of the cache, merges its warps' partial
+// softmaxes in shared memory, and either writes the output (one split) or an
+// fp32 partial (m, l, o[d]) that a second kernel merges.
+
+#include "ptx.cuh"
+
+namespace alibi {
+namespace {
+
+constexpr int kDecodeD = 128;
+constexpr int kWarps = 8;
+constexpr int kKeysPerHalf = 8;               // keys per half-warp per step
+constexpr int kKeysPerWarp = 2 * kKeysPerHalf;  // 16
+constexpr int kPartStride = kDecodeD + 4;     // floats per partial: m, l, pad, pad, o[d]
+
+struct DecodeParams {
+    const __nv_bfloat16 *q, *k, *v;
+    __nv_bfloat16 *out;
+    float *part;  // [BH][splits][kPartStride], used when splits > 1
+    int H, L, splits, chunk;
+    float c1;  // log2(e) / sqrt(d)
+    Slopes slopes;
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        f[2 * t] = __uint_as_float(w[t] << 16);
+        f[2 * t + 1] = __uint_as_float(w[t] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_constant__ DecodeParams p)
+{
+    __shared__ float sm_m[kWarps], sm_l[kWarps];
+    __shared__ float sm_o[kWarps][kDecodeD];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane >> 4, l16 = lane & 15;
+    const int bh = blockIdx.y, split = blockIdx.x;
+    const int h = bh % p.H;
+    const float sl2 = p.slopes.log2e[h];
+    const int pos = p.L - 1;
+    const int kbeg = split * p.chunk;
+    const int kend = min(p.L, kbeg + p.chunk);
+
+    // this lane's 8 query elements (d slice [8 l16, 8 l16 + 8)), pre-scaled to log2 units
+    float qf[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(p.q + static_cast<size_t>(bh) * kDecodeD + 8 * l16), qf);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) qf[t] *= p.c1;
+
+    const __nv_bfloat16 *kbase = p.k + static_cast<size_t>(bh) * p.L * kDecodeD + 8 * l16;
+    const __nv_bfloat16 *vbase = p.v + static_cast<size_t>(bh) * p.L * kDecodeD + 8 * l16;
+
+    float m = -INFINITY, l = 0.f, o[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) o[t] = 0.f;
+
+    for (int blk = kbeg + warp * kKeysPerWarp; blk < kend; blk += kWarps * kKeysPerWarp) {
+        uint4 kr[kKeysPerHalf], vr[kKeysPerHalf];
+#pragma unroll
+        for (int u = 0; u < kKeysPerHalf; ++u) {
+            const int key = blk + 2 * u + half;
+            if (key < kend) {
+                kr[u] = ld_stream(kbase + static_cast<size_t>(key) * kDecodeD);
+                vr[u] = ld_stream(vbase + static_cast<size_t>(key) * kDecodeD);
+            } else {
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float x[kKeysPerHalf];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kKeysPerHalf; ++u) {
+            float kf[8];
+            bf16x8_to_f32(kr[u], kf);
+            float dot = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) dot = fmaf(qf[t], kf[t], dot);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 8);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            const int key = blk + 2 * u + half;
+            x[u] = (key < kend) ? fmaf(-sl2, static_cast<float>(pos - key), dot) : -INFINITY;
+            mt = fmaxf(mt, x[u]);
+        }
+        if (mt > -INFINITY) {  // this half-warp saw at least one key in range
+            const float mn = fmaxf(m, mt);
+            const float alpha = ex2_approx(m - mn);  // 0 while m is still -inf
+            m = mn;
+            l *= alpha;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) o[t] *= alpha;
+#pragma unroll
+            for (int u = 0; u < kKeysPerHalf; ++u) {
+                const float pu = ex2_approx(x[u] - m);
+                l += pu;
+                float vf[8];
+                bf16x8_to_f32(vr[u], vf);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) o[t] = fmaf(pu, vf[t], o[t]);
+            }
+        }
+    }
+
+    // merge the two half-warps (lanes l16 and l16 + 16 own the same d slice)
+    {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, 16);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, 16);
+        const float mn = fmaxf(m, mo);
+        const float a = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+        const float b = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mn);
+        l = l * a + lo * b;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float oo = __shfl_xor_sync(0xffffffffu, o[t], 16);
+            o[t] = o[t] * a + oo * b;
+        }
+        m = mn;
+    }
+    if (lane < 16) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sm_o[warp][8 * l16 + t] = o[t];
+        if (lane == 0) {
+            sm_m[warp] = m;
+            sm_l[warp] = l;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < kDecodeD) {
+        const int t = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w]);
+        float Lsum = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float a = (sm_m[w] == -INFINITY) ? 0.f : ex2_approx(sm_m[w] - M);
+            Lsum = fmaf(sm_l[w], a, Lsum);
+            O = fmaf(sm_o[w][t], a, O);
+        }
+        if (p.splits == 1) {
+            p.out[static_cast<size_t>(bh) * kDecodeD + t] = __float2bfloat16_rn(O / Lsum);
+        } else {
+            float *dst = p.part + (static_cast<size_t>(bh) * p.splits + split) * kPartStride;
+            if (t == 0) {
+                dst[0] = M;
+                dst[1] = Lsum;
+            }
+            dst[4 + t] = O;
+        }
+    }
+}
+
+// One warp per (b, h): merge the splits' partial softmaxes.
+__global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restrict__ part,
+                                                           __nv_bfloat16 *__restrict__ out, int BH, int splits)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= BH) return;
+    const float *base = part + static_cast<size_t>(warp) * splits * kPartStride;
+    float M = -INFINITY;
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, base[s * kPartStride]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < splits; ++s) {
+        const float *ps = base + s * kPartStride;
+        const float ms = ps[0];
+        const float a = (ms == -INFINITY) ? 0.f : ex2_approx(ms - M);
+        Lsum = fmaf(ps[1], a, Lsum);
+        const float4 ov = *reinterpret_cast<const float4 *>(ps + 4 + 4 * lane);
+        O[0] = fmaf(ov.x, a, O[0]);
+        O[1] = fmaf(ov.y, a, O[1]);
+        O[2] = fmaf(ov.z, a, O[2]);
+        O[3] = fmaf(ov.w, a, O[3]);
+    }
+    const float inv = 1.0f / Lsum;
+    __nv_bfloat162 r0 = __floats2bfloat162_rn(O[0] * inv, O[1] * inv);
+    __nv_bfloat162 r1 = __floats2bfloat162_rn(O[2] * inv, O[3] * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&r0);
+    pk.y = *reinterpret_cast<uint32_t *>(&r1);
+    *reinterpret_cast<uint2 *>(out + static_cast<size_t>(warp) * kDecodeD + 4 * lane) = pk;
+}
+
+}  // namespace
+
+// Split count: enough CTAs for several waves (two resident per SM), at least
+// 512 keys per split, and every split non-empty.
+int decode_splits(int BH, int L)
+{
+    const int target = 8 * 2 * num_sms();
+    int splits = (target + BH - 1) / BH;
+    const int max_by_len = (L + 511) / 512;
+    if (splits > max_by_len) splits = max_by_len;
+    if (splits < 1) splits = 1;
+    return splits;
+}
+
+size_t decode_partials_bytes(int BH, int splits)
+{
+    return splits > 1 ? static_cast<size_t>(BH) * splits * kPartStride * sizeof(float) : 0;
+}
+
+cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L,
+                               const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
+{
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(kc);
+    p.v = static_cast<const __nv_bfloat16 *>(vc);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.part = partials;
+    p.H = H;
+    p.L = L;
+    p.splits = splits;
+    p.chunk = (L + splits - 1) / splits;
+    p.chunk = (p.chunk + kKeysPerWarp - 1) / kKeysPerWarp * kKeysPerWarp;
+    p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(kDecodeD));
+    p.slopes = slopes;
+    const int BH = B * H;
+    // recompute splits so that no split is empty after rounding the chunk
+    p.splits = (L + p.chunk - 1) / p.chunk;
+    if (p.splits > splits) return cudaErrorInvalidValue;
+    dim3 grid(p.splits, BH);
+    decode_kernel<<<grid, kWarps * 32, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.splits == 1) return e;
+    decode_merge_kernel<<<(BH + 3) / 4, 128, 0, stream>>>(partials, p.out, BH, p.splits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
+                          const Slopes &slopes, cudaStream_t stream)
+{
+    if (d != kDecodeD) return cudaErrorInvalidValue;
+    const int BH = B * H;
+    const int splits = decode_splits(BH, L);
+    if (splits == 1) return launch_decode_with(q, kc, vc, out, B, H, L, slopes, 1, nullptr, stream);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, decode_partials_bytes(BH, splits), decode_pool(), stream);
+    if (e != cudaSuccess) return e;
+    e = launch_decode_with(q, kc, vc, out, B, H, L, slopes, splits, static_cast<float *>(ws), stream);
+    cudaError_t f = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : f;
+}
+
+}  // namespace alibi

@@ -1,0 +1,444 @@
+// Causal ALiBi prefill on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes, per (b, h) and query row i,
+//   x_ij = q_i.k_j / sqrt(d) - m_h (i - j)   for j <= i        (keys j > i masked)
+//   O_i  = sum_j softmax_j(x_ij) v_j,   LSE_i = ln sum_j exp(x_ij)
+// following "When Attention Goes Blind: Numerical Failure in ALiBi Positional
+// Encodings" (arXiv 2608.03994) sec. 3.1 eq. 1-3 and App. B.1 (max-shifted
+// softmax), and "ALiBi: Attention with Linear Biases" (abhik.ai), "From
+// distance to a normalized weight" and the remark after the full-sequence
+// example that a production kernel generates the biases inside its tiles.
+//
+// Design (one persistent CTA per SM, 384 threads):
+//   warp 0      TMA producer: Q tiles once per work item, K/V tiles through
+//               two 2-stage rings (128-byte swizzle, zero fill past N).
+//   warp 1      TMEM allocator and single-thread MMA issuer:
+//                 S_s = Q_s K^T   (128 x 128, fp32 in TMEM, smem x smem)
+//                 O_s += P_s V    (128 x d,   fp32 in TMEM, P read from TMEM)
+//   warps 4-7   softmax for Q tile slot 0, warps 8-11 for slot 1: each thread
+//               owns one query row (tcgen05.ld gives a thread a whole TMEM
+//               lane), so the row max and row sum need no shuffles. The bias
+//               is generated from the integer tile coordinates; the running
+//               max is raised lazily (only when a tile exceeds it by 2^8).
+// A work item is (b*H + h, block of 256 query rows = two 128-row tiles);
+// KV tiles are visited from the diagonal downwards and tiles entirely above
+// the diagonal are never loaded. Items are dealt longest-first in snake order.
+//
+// TMEM columns: S/P slot s at [128 s, 128 s + 128), O slot s at 256 + 128 s.
+// P (bf16, two per 32-bit column) overwrites the first 64 columns of S.
+
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace alibi {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (MMA M)
+constexpr int BN = 128;  // keys per tile
+constexpr int kThreads = 384;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along d
+    static constexpr uint32_t kChunkBytes = BM * 128;      // one 64-column box: 16 KB
+    static constexpr uint32_t kTileBytes = BM * D * 2;     // one 128 x D bf16 tile
+    static constexpr uint32_t kQ = 0;                      // 2 Q tiles
+    static constexpr uint32_t kK = 2 * kTileBytes;         // K ring
+    static constexpr uint32_t kV = kK + kKStages * kTileBytes;  // V ring
+    static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
+    static constexpr uint32_t kSmem = kBar + 256 + 1024;   // barriers, TMEM slot, alignment slack
+};
+
+struct FwdParams {
+    CUtensorMap tq, tk, tv;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
+    __nv_bfloat16 *out;
+    float *lse;
+    uint32_t *err;
+    int N, BH, H, NQB, NQT, num_items;
+    float c1;  // log2(e) / sqrt(d)
+    Slopes slopes;
+};
+
+enum : uint32_t {
+    SITE_PROD_Q = 0x101, SITE_PROD_K = 0x102, SITE_PROD_V = 0x103,
+    SITE_MMA_Q = 0x201, SITE_MMA_K = 0x202, SITE_MMA_V = 0x203, SITE_MMA_P = 0x204, SITE_MMA_O = 0x205,
+    SITE_MMA_DONE = 0x206, SITE_SM_S = 0x301, SITE_SM_O = 0x302,
+};
+
+struct Item {
+    int bh, qb, n;
+    bool q1valid;
+};
+
+__device__ __forceinline__ int item_index(int k)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    return (k & 1) ? (k + 1) * G - 1 - c : k * G + c;
+}
+
+__device__ __forceinline__ Item decode_item(const FwdParams &p, int w)
+{
+    Item it;
+    const int round = w / p.BH;
+    it.bh = w - round * p.BH;
+    it.qb = p.NQB - 1 - round;
+    const int qt1 = 2 * it.qb + 1;
+    it.q1valid = qt1 < p.NQT;
+    it.n = it.q1valid ? qt1 + 1 : qt1;  // KV tiles 0 .. n-1
+    return it;
+}
+
+// Is Q slot s active at iteration `it` (KV tile n-1-it)?
+__device__ __forceinline__ bool slot_active(const Item &t, int s, int it)
+{
+    return s == 1 ? t.q1valid : (t.q1valid ? it >= 1 : true);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBar);
+    uint64_t *q_full = bars + 0;    // [2]
+    uint64_t *q_empty = bars + 2;   // [1]
+    uint64_t *k_full = bars + 3;    // [2]
+    uint64_t *k_empty = bars + 5;   // [2]
+    uint64_t *v_full = bars + 7;    // [2]
+    uint64_t *v_empty = bars + 9;   // [2]
+    uint64_t *s_full = bars + 11;   // [2]
+    uint64_t *p_full = bars + 13;   // [2]
+    uint64_t *o_full = bars + 15;   // [2]
+    uint64_t *o_empty = bars + 17;  // [2]
+    uint64_t *mma_done = bars + 19; // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint32_t *err = p.err;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 128);
+            mbar_init(&o_full[s], 1);
+            mbar_init(&o_empty[s], 128);
+        }
+        mbar_init(q_empty, 1);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tq);
+        tma_prefetch_desc(&p.tk);
+        tma_prefetch_desc(&p.tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t kc = 0, vc = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = item_index(k);
+                if (w >= p.num_items) break;
+                const Item t = decode_item(p, w);
+                ok = mbar_wait(q_empty, (k & 1) ^ 1, err, SITE_PROD_Q);
+                if (!ok) break;
+                for (int s = 0; s < 2; ++s) {
+                    mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem + C::kQ + s * C::kTileBytes + c * C::kChunkBytes, &p.tq, 64 * c,
+                                    (2 * t.qb + s) * BM, t.bh, &q_full[s]);
+                }
+                auto load_kv = [&](const CUtensorMap *map, uint32_t base, uint64_t *full, uint64_t *empty,
+                                   uint32_t &cnt, int jtile, uint32_t site) -> bool {
+                    const uint32_t st = cnt % 2, ph = (cnt / 2) & 1;
+                    if (!mbar_wait(&empty[st], ph ^ 1, err, site)) return false;
+                    mbar_arrive_expect_tx(&full[st], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem + base + st * C::kTileBytes + c * C::kChunkBytes, map, 64 * c, jtile * BN,
+                                    t.bh, &full[st]);
+                    ++cnt;
+                    return true;
+                };
+                // order: K(0), K(1), V(0), K(2), V(1), ..., V(n-1)
+                for (int it = 0; it < t.n && ok; ++it) {
+                    ok = load_kv(&p.tk, C::kK, k_full, k_empty, kc, t.n - 1 - it, SITE_PROD_K);
+                    if (ok && it >= 1) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, t.n - it, SITE_PROD_V);
+                }
+                if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, 0, SITE_PROD_V);
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
+            const uint32_t sQ = smem_u32(smem + C::kQ);
+            const uint32_t sK = smem_u32(smem + C::kK);
+            const uint32_t sV = smem_u32(smem + C::kV);
+            uint32_t kc = 0, vc = 0;
+            uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = item_index(k);
+                if (w >= p.num_items) break;
+                const Item t = decode_item(p, w);
+                const int last_slot = t.q1valid ? 1 : 0;
+                ok = mbar_wait(&q_full[0], k & 1, err, SITE_MMA_Q) && mbar_wait(&q_full[1], k & 1, err, SITE_MMA_Q);
+                if (!ok) break;
+                tc_fence_after();
+
+                // S_s = Q_s K^T over d in steps of 16 (K-major operands, 32-byte steps inside a swizzle atom)
+                auto issue_S = [&](int s, uint32_t kst) {
+                    const uint32_t qa = sQ + s * C::kTileBytes, kb = sK + kst * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                        mma_ss(tmem + s * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                               idS, kk > 0);
+                    }
+                    mma_commit(&s_full[s]);
+                };
+                // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous)
+                auto issue_PV = [&](int s, uint32_t vst, bool first) {
+                    const uint32_t vb = sV + vst * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(tmem + 256 + s * 128, tmem + s * 128 + kk * 8,
+                               smem_desc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), idO, (first && kk == 0) ? 0u : 1u);
+                };
+
+                bool first_pv[2] = {true, true};
+                // prologue: K(0) and the S of slots active at it = 0
+                {
+                    const uint32_t st = kc % 2, ph = (kc / 2) & 1;
+                    ok = mbar_wait(&k_full[st], ph, err, SITE_MMA_K);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int s = 0; s < 2; ++s)
+                        if (slot_active(t, s, 0)) issue_S(s, st);
+                    mma_commit(&k_empty[st]);
+                }
+                int k_ready = 0;  // highest iteration whose K tile has been waited for
+                for (int it = 0; it < t.n && ok; ++it) {
+                    const uint32_t vst = (vc + it) % 2, vph = ((vc + it) / 2) & 1;
+                    ok = mbar_wait(&v_full[vst], vph, err, SITE_MMA_V);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int s = 0; s < 2 && ok; ++s) {
+                        if (slot_active(t, s, it)) {
+                            ok = mbar_wait(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
+                            ++p_cnt[s];
+                            if (ok && first_pv[s]) ok = mbar_wait(&o_empty[s], (o_cnt[s] & 1) ^ 1, err, SITE_MMA_O);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_PV(s, vst, first_pv[s]);
+                            first_pv[s] = false;
+                            if (it == t.n - 1) {
+                                mma_commit(&o_full[s]);
+                                ++o_cnt[s];
+                            }
+                        }
+                        if (it + 1 < t.n && slot_active(t, s, it + 1)) {
+                            const uint32_t kst = (kc + it + 1) % 2, kph = ((kc + it + 1) / 2) & 1;
+                            if (k_ready < it + 1) {
+                                ok = mbar_wait(&k_full[kst], kph, err, SITE_MMA_K);
+                                if (!ok) break;
+                                tc_fence_after();
+                                k_ready = it + 1;
+                            }
+                            issue_S(s, kst);
+                            if (s == last_slot) mma_commit(&k_empty[kst]);
+                        }
+                    }
+                    mma_commit(&v_empty[vst]);
+                }
+                mma_commit(q_empty);
+                kc += t.n;
+                vc += t.n;
+            }
+            // drain: every MMA issued above completes before TMEM is released
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, err, SITE_MMA_DONE);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ softmax warpgroups
+        const int s = (warp - 4) >> 2;
+        const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        uint32_t s_cnt = 0, o_cnt = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int w = item_index(k);
+            if (w >= p.num_items) break;
+            const Item t = decode_item(p, w);
+            if (s == 1 && !t.q1valid) continue;
+            const int qt = 2 * t.qb + s;
+            const int i = qt * BM + r;
+            const float sl2 = p.slopes.log2e[t.bh % p.H];
+            const int it0 = (s == 0 && t.q1valid) ? 1 : 0;
+            float M = -INFINITY, l = 0.f;
+            for (int it = it0; it < t.n; ++it) {
+                const int j = t.n - 1 - it;
+                ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_SM_S);
+                ++s_cnt;
+                if (!ok) break;
+                tc_fence_after();
+                float x[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    tmem_ld32(lane_addr + s * 128 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+                tmem_wait_ld();
+                // x = s * log2(e)/sqrt(d) - m log2(e) (i - j), from the integer offset i - k0
+                const float nb = -sl2 * static_cast<float>(i - j * BN);
+                float mt = -INFINITY;
+                if (j == qt) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) {
+                        const float b = fmaf(sl2, static_cast<float>(c), nb);
+                        x[c] = (c > r) ? -INFINITY : fmaf(x[c], p.c1, b);
+                        mt = fmaxf(mt, x[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) {
+                        x[c] = fmaf(x[c], p.c1, fmaf(sl2, static_cast<float>(c), nb));
+                        mt = fmaxf(mt, x[c]);
+                    }
+                }
+                if (it == it0) {
+                    M = mt;
+                } else if (mt > M + kRescaleThreshold) {
+                    // raise the running max; O_s is quiescent: S_s(it) completing implies PV_s(it-1) did
+                    const float alpha = ex2_approx(M - mt);
+                    M = mt;
+                    l *= alpha;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_addr + 256 + s * 128 + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                        tmem_st32(lane_addr + 256 + s * 128 + c * 32, o);
+                    }
+                }
+                float sum = 0.f;
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int u = 0; u < BN / 2; ++u) {
+                    const float p0 = ex2_approx(x[2 * u] - M);
+                    const float p1 = ex2_approx(x[2 * u + 1] - M);
+                    sum += p0 + p1;
+                    pk[u] = pack_bf16x2(p0, p1);
+                }
+                l += sum;
+                tmem_st32(lane_addr + s * 128, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(lane_addr + s * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[s]);
+            }
+            if (!ok) break;
+            // ------------------------------------------------------ epilogue
+            ok = mbar_wait(&o_full[s], o_cnt & 1, err, SITE_SM_O);
+            ++o_cnt;
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = 1.0f / l;
+            const bool valid = i < p.N;
+            __nv_bfloat16 *orow = p.out + (static_cast<size_t>(t.bh) * p.N + (valid ? i : 0)) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + 256 + s * 128 + c * 32, o);
+                tmem_wait_ld();
+                uint32_t b[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv_l, __uint_as_float(o[2 * u + 1]) * inv_l);
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&o_empty[s]);
+            if (valid && p.lse) p.lse[static_cast<size_t>(t.bh) * p.N + i] = (M + __log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                                   int H, int N, const Slopes &slopes, cudaStream_t stream)
+{
+    using C = Cfg<D>;
+    FwdParams p;
+    const uint64_t BH = static_cast<uint64_t>(B) * H;
+    if (!encode_tmap_bf16_3d(&p.tq, q, D, N, BH, 64, BM) || !encode_tmap_bf16_3d(&p.tk, k, D, N, BH, 64, BN) ||
+        !encode_tmap_bf16_3d(&p.tv, v, D, N, BH, 64, BN))
+        return cudaErrorInvalidValue;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.err = device_status_word();
+    if (!p.err) return cudaErrorInvalidDevice;
+    p.N = N;
+    p.BH = static_cast<int>(BH);
+    p.H = H;
+    p.NQT = (N + BM - 1) / BM;
+    p.NQB = (p.NQT + 1) / 2;
+    p.num_items = p.NQB * p.BH;
+    p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.slopes = slopes;
+
+    static bool attr_set = false;  // per process; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+    fwd_tc_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
+                          int d, const Slopes &slopes, cudaStream_t stream)
+{
+    if (d == 128) return launch_fwd_tc_d<128>(q, k, v, out, lse, B, H, N, slopes, stream);
+    if (d == 64) return launch_fwd_tc_d<64>(q, k, v, out, lse, B, H, N, slopes, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace alibi

@@ -1,0 +1,288 @@
+// Host side of the C ABI declared in include/alibi.h: argument validation,
+// the ALiBi slope schedule, TMA tensor-map encoding, per-device state (status
+// word, SM count, decode memory pool) and the extern "C" entry points.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "alibi.h"
+#include "internal.h"
+
+namespace alibi {
+
+// Device status word: [0] = ALIBI_DEV_* bits, [1] = first failing site.
+__device__ uint32_t g_status[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t *g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Slope exponent of head h as 2^(-num/den): "ALiBi: Attention with Linear
+// Biases" (abhik.ai), "Different heads, different distance penalties".
+void slope_exponent(int H, int h, int *num, int *den)
+{
+    int c = 1;
+    while (c * 2 <= H) c *= 2;  // largest power of two <= H
+    if (h < c) {
+        *num = 8 * (h + 1);
+        *den = c;
+    } else {
+        *num = 8 * (2 * (h - c) + 1);  // every other entry of the 2c schedule
+        *den = 2 * c;
+    }
+}
+
+// 2^(-num/den) rounded once to fp32: the integer part of the exponent is
+// applied exactly with ldexp, the fractional part in long double.
+float slope_value(int num, int den)
+{
+    const int whole = num / den, frac = num % den;
+    const long double f = exp2l(-static_cast<long double>(frac) / static_cast<long double>(den));
+    return static_cast<float>(ldexpl(f, -whole));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int to_status(cudaError_t e)
+{
+    return e == cudaSuccess ? ALIBI_OK : ALIBI_ERR_CUDA;
+}
+
+}  // namespace
+
+uint32_t *device_status_word()
+{
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<uint32_t *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int num_sms()
+{
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+cudaMemPool_t decode_pool()
+{
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        // keep freed blocks in this pool: the partials buffer is reused call after call
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pool[dev] = pool;
+    }
+    return g_pool[dev];
+}
+
+void fill_slopes(int H, Slopes *s)
+{
+    for (int h = 0; h < H && h < kMaxHeads; ++h) {
+        int num, den;
+        slope_exponent(H, h, &num, &den);
+        s->nat[h] = slope_value(num, den);
+        s->log2e[h] = static_cast<float>(static_cast<double>(s->nat[h]) * 1.4426950408889634);
+    }
+}
+
+bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                         uint32_t box0, uint32_t box1)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {dim0, dim1, dim2};
+    const cuuint64_t strides[2] = {dim0 * 2, dim0 * dim1 * 2};  // bytes, dims 1 and 2
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace alibi
+
+using namespace alibi;
+
+extern "C" {
+
+int alibi_version(void) { return 100; }
+
+const char *alibi_status_str(int status)
+{
+    switch (status) {
+        case ALIBI_OK: return "ALIBI_OK";
+        case ALIBI_ERR_INVALID: return "ALIBI_ERR_INVALID: invalid argument";
+        case ALIBI_ERR_UNSUPPORTED: return "ALIBI_ERR_UNSUPPORTED: unsupported shape or option";
+        case ALIBI_ERR_CUDA: return "ALIBI_ERR_CUDA: CUDA call or kernel launch failed";
+        case ALIBI_ERR_TIMEOUT: return "ALIBI_ERR_TIMEOUT: a bounded device-side wait expired";
+        default: return "unknown alibi status";
+    }
+}
+
+int alibi_slopes(int H, float *out_host)
+{
+    if (!out_host || H < 1 || H > 4096) return ALIBI_ERR_INVALID;
+    for (int h = 0; h < H; ++h) {
+        int num, den;
+        slope_exponent(H, h, &num, &den);
+        out_host[h] = slope_value(num, den);
+    }
+    return ALIBI_OK;
+}
+
+static int check_dims(int B, int H, int N, int d)
+{
+    if (B < 1 || H < 1 || N < 1 || d < 1) return ALIBI_ERR_INVALID;
+    if (H > kMaxHeads) return ALIBI_ERR_UNSUPPORTED;
+    // flat indices stay below 2^31 rows per (b, h) and 2^24 positions (exact in fp32)
+    if (N > (1 << 24) || static_cast<long long>(B) * H > (1LL << 31) - 1) return ALIBI_ERR_UNSUPPORTED;
+    return ALIBI_OK;
+}
+
+int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
+                   int causal, void *stream)
+{
+    if (!q || !k || !v || !out) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && !aligned16(lse)))
+        return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
+    if (causal == 0) return ALIBI_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_fwd_tc(q, k, v, out, lse, B, H, N, d, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B, int H, int N,
+                       int d, int causal, void *stream)
+{
+    if (!q || !k || !v || !out) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && !aligned16(lse)))
+        return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
+    if (causal == 0) return ALIBI_ERR_UNSUPPORTED;
+    if (d > 256) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_fwd_f32(q, k, v, out, lse, B, H, N, d, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_decode(const void *q, const void *kcache, const void *vcache, void *out, int B, int H, int L, int d,
+                      void *stream)
+{
+    if (!q || !kcache || !vcache || !out) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out)) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, L, d);
+    if (st != ALIBI_OK) return st;
+    if (d != 128) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_decode(q, kcache, vcache, out, B, H, L, d, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_decode_splits(int B, int H, int L, int d)
+{
+    int st = check_dims(B, H, L, d);
+    if (st != ALIBI_OK) return st;
+    if (d != 128) return ALIBI_ERR_UNSUPPORTED;
+    return decode_splits(B * H, L);
+}
+
+int alibi_attn_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N, int d,
+                         void *stream)
+{
+    if (!q || !k || !lse || !P) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (d > 256) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_probs_f32(q, k, lse, P, B, H, N, d, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N, int d, float tau,
+                              unsigned long long *counts, void *stream)
+{
+    if (!q || !k || !counts) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(counts) & 7u)) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (!std::isfinite(tau)) return ALIBI_ERR_INVALID;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_underflow(q, k, B, H, N, d, tau, counts, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_check_error(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ALIBI_ERR_CUDA;
+    uint32_t *w = device_status_word();
+    if (!w) return ALIBI_ERR_CUDA;
+    uint32_t h[2] = {0, 0};
+    if (cudaMemcpy(h, w, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ALIBI_ERR_CUDA;
+    if (h[0] != 0u && cudaMemset(w, 0, sizeof(h)) != cudaSuccess) return ALIBI_ERR_CUDA;
+    if (h[0] & ALIBI_DEV_TIMEOUT) return ALIBI_ERR_TIMEOUT;
+    if (h[0] != 0u) return ALIBI_ERR_CUDA;
+    return ALIBI_OK;
+}
+
+}  // extern "C"

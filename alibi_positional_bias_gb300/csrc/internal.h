@@ -1,0 +1,51 @@
+// Internal declarations shared by the host entry points and the kernel units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace alibi {
+
+// Device status word bits (word 0) and the first failing site (word 1).
+constexpr uint32_t ALIBI_DEV_TIMEOUT = 1u;
+constexpr uint32_t ALIBI_DEV_BADSTATE = 2u;
+
+// Every device-side wait gives up after this long (ns).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Largest head count the kernels accept (slopes travel as kernel parameters).
+constexpr int kMaxHeads = 256;
+
+struct Slopes {
+    float log2e[kMaxHeads];  // m_h * log2(e): the bias in base-2 exponent units
+    float nat[kMaxHeads];    // m_h in natural-log units
+};
+
+// Host helpers (alibi_host.cu).
+uint32_t *device_status_word();  // per current device, 2 words
+void fill_slopes(int H, Slopes *s);
+int num_sms();                   // of the current device
+cudaMemPool_t decode_pool();     // library-owned stream-ordered pool of the current device
+// 3-D TMA map over a [dim2, dim1, dim0] bf16 tensor (dim0 fastest), box {box0, box1, 1},
+// 128-byte swizzle, zero fill out of bounds.
+bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                         uint32_t box0, uint32_t box1);
+
+// Decode split plan (alibi_decode.cu): number of KV splits for B*H heads of length L.
+int decode_splits(int BH, int L);
+
+// Kernel launchers; each returns a cudaError_t from the launch.
+cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                          int N, int d, const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B,
+                           int H, int N, int d, const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N,
+                             int d, const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
+                          const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_underflow(const void *q, const void *k, int B, int H, int N, int d, float tau,
+                             unsigned long long *counts, const Slopes &slopes, cudaStream_t stream);
+
+}  // namespace alibi

@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark of the ALiBi causal attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill: alibi_attn_fwd on the long-context workload (B=1, H=16,
+    N=16384, d=128, bf16; Q, K ~ N(0, 1), V ~ U(-1, 1)), causal, fp32 LSE;
+  * decode: alibi_attn_decode on B=64 sequences, H=40, one query each at
+    position L-1 against a bf16 KV cache of L=8192, d=128.
+The headline ``value`` is prefill TFLOP/s with the causal count 2 B H N^2 d;
+decode reports KV GB/s (2 B H L d bytes of bf16 cache per call).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path shards over (b, h) with no exchange step): weak scaling, the barrier and
+the max-over-ranks time stay.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = "long_n16384"
+DECODE = "decode_l8192"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def prefill_flops(w) -> float:
+    return 2.0 * w.B * w.H * w.N * w.N * w.d
+
+
+def decode_bytes(w) -> float:
+    return 2.0 * w.B * w.H * w.N * w.d * 2.0
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples (200 ms) during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU (oracle)
+
+def oracle_prefill_sample(w, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on sampled rows of the prefill workload. Returns
+    (causal FLOPs of the rows, seconds, rows, threads)."""
+    import numpy as np
+    import alibi_inputs as gen
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    threads = os.cpu_count() or 1
+    m = oracle.slopes(w.H)
+    # one head's Q, K, V (regenerated independently); rows spread over positions
+    h = int(rng.integers(0, w.H))
+    q, k, v = (gen.head_slice(w, i, 0, h) for i in range(3))
+    qh, kh, vh = (t.f32[None, None] for t in (q, k, v))
+    flops, secs, nrows = 0.0, 0.0, 0
+    batch = max(threads * 2, 16)
+    while secs < budget_s:
+        rows = np.sort(rng.integers(0, w.N, size=batch))
+        t0 = time.perf_counter()
+        oracle.attention(qh, kh, vh, m=m[h:h + 1], rows=rows, nthreads=threads)
+        secs += time.perf_counter() - t0
+        flops += float(np.sum(4.0 * (rows + 1) * w.d))
+        nrows += len(rows)
+    return flops, secs, nrows, threads
+
+
+def oracle_decode_sample(w, budget_s: float, seed: int = 1):
+    import numpy as np
+    import alibi_inputs as gen
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    threads = os.cpu_count() or 1
+    m = oracle.slopes(w.H)
+    nbytes, secs, heads = 0.0, 0.0, 0
+    while secs < budget_s:
+        qs, ks, vs = [], [], []
+        picks = [(int(rng.integers(0, w.B)), int(rng.integers(0, w.H))) for _ in range(max(threads, 4))]
+        for b, h in picks:
+            qs.append(gen.head_slice(w, 0, b, h).f32)
+            ks.append(gen.head_slice(w, 1, b, h).f32)
+            vs.append(gen.head_slice(w, 2, b, h).f32)
+        hh = [h for _, h in picks]
+        Q = np.stack(qs)[None]
+        K = np.stack(ks)[None]
+        V = np.stack(vs)[None]
+        # each picked (b, h) is one "head" of a B=1 problem with its own slope
+        t0 = time.perf_counter()
+        oracle.decode(Q, K, V, m=m[hh], nthreads=threads)
+        secs += time.perf_counter() - t0
+        nbytes += len(picks) * 2.0 * w.N * w.d * 2.0
+        heads += len(picks)
+    return nbytes, secs, heads, threads
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, timed as it stands on the host cores."""
+    import alibi_inputs as gen
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    wp = gen.WORKLOADS[PREFILL]
+    per_step = 3.0
+    for _ in range(args.warmup):
+        oracle_prefill_sample(wp, 0.5)
+    flops, secs, rows, threads = 0.0, 0.0, 0, 1
+    for _ in range(args.steps):
+        f, s, r, threads = oracle_prefill_sample(wp, per_step, seed=rows)
+        flops += f
+        secs += s
+        rows += r
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": "ALiBi causal attention fwd TFLOP/s (% bf16 TC peak); decode KV GB/s (% HBM)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{PREFILL} (B=1, H=16, N=16384, d=128, causal) prefill rows, fp64 oracle",
+                   "global_batch": wp.B, "seq_len": wp.N, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} query rows of one head of {PREFILL}, spread over positions; "
+                                   f"~{per_step:.0f} s of CPU work per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- native
+
+def run_native(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import alibi_inputs as gen
+    import alibi_positional_bias_gb300 as ab
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ab.load(build_if_missing=True)
+    peaks = load_peaks()
+    wp, wd = gen.WORKLOADS[PREFILL], gen.WORKLOADS[DECODE]
+
+    # inputs resident in HBM before the timed region
+    q = torch.empty(wp.shapes()[0], dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty_like(q)
+    for i, t in enumerate((q, k, v)):
+        gen.fill_device(wp, i, t)
+    out = torch.empty_like(q)
+    lse = torch.empty((wp.B, wp.H, wp.N), dtype=torch.float32, device=dev)
+    dq = torch.empty(wd.shapes()[0], dtype=torch.bfloat16, device=dev)
+    dk = torch.empty(wd.shapes()[1], dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    for i, t in enumerate((dq, dk, dv)):
+        gen.fill_device(wd, i, t)
+    dout = torch.empty_like(dq)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    splits = ab.alibi_attn_decode_splits(wd.B, wd.H, wd.N, wd.d)
+    launches_per_step = 1 + (2 if splits > 1 else 1)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        flush.fill_(1.0)  # L2 flush, outside the event-timed launches
+        if evs:
+            evs[0].record(stream)
+        ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        ab.alibi_attn_decode(dq, dk, dv, out=dout, stream=stream)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    ab.alibi_check_error(stream)
+
+    sampler = ClockSampler(dev.index)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        step(events[s])
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ab.alibi_check_error(stream)
+
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in events)  # ms
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in events)
+    times = torch.tensor([t_pre, t_dec], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    t_pre, t_dec = float(times[0]), float(times[1])
+    K = args.steps
+    pre_launch_s = t_pre / 1e3 / K
+    dec_launch_s = t_dec / 1e3 / K
+    value = world * prefill_flops(wp) * K / (t_pre / 1e3) / 1e12
+    dec_gbs = world * decode_bytes(wd) * K / (t_dec / 1e3) / 1e9
+
+    # ------------------------------------------------ end to end (host buffers)
+    e2e = None
+    e2e_dec = None
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        hk = k.cpu().pin_memory()
+        hv = v.cpu().pin_memory()
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        ke = min(K, 5)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * prefill_flops(wp) * ke / (float(t[0]) / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
+               "steps": ke}
+        # decode: the cache stays resident (it is state, not a per-step input); the
+        # new query goes up and the output comes back every step
+        hdq = dq.cpu().pin_memory()
+        hdo = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+        e0.record(stream)
+        for _ in range(ke):
+            dq.copy_(hdq, non_blocking=True)
+            ab.alibi_attn_decode(dq, dk, dv, out=dout, stream=stream)
+            hdo.copy_(dout, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_dec = {"value": world * decode_bytes(wd) * ke / (float(t[0]) / 1e3) / 1e9, "unit": "GB/s",
+                   "h2d_bytes_per_step": dq.numel() * 2, "d2h_bytes_per_step": dout.numel() * 2}
+        ab.alibi_check_error(stream)
+
+    # ------------------------------------------ underflow fraction (reported, untimed)
+    tau = math.log(2.0 ** -126)
+    counts = ab.alibi_attn_underflow_bf16(q, k, tau).cpu().numpy().astype(np.float64)
+    pairs_per_head = wp.B * wp.N * (wp.N + 1) / 2
+    underflow = {"tau": "ln 2^-126", "fraction": float(counts.sum() / (pairs_per_head * wp.H)),
+                 "per_head": [round(float(c / pairs_per_head), 4) for c in counts]}
+
+    # ------------------------------------------------------ CPU baseline (oracle)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, s, rows, threads = oracle_prefill_sample(wp, args.cpu_seconds)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} query rows of one head of {PREFILL} (causal FLOPs 4 (i+1) d per row), "
+                         f"fp64, {s:.1f} s"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    traffic = load_traffic()
+    line = {
+        "metric": "ALiBi causal attention fwd TFLOP/s (% bf16 TC peak); decode KV GB/s (% HBM)",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": (t_pre + t_dec) / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{PREFILL}: prefill B=1 H=16 N=16384 d=128 causal (Q,K~N(0,1), V~U(-1,1)) + "
+                        f"{DECODE}: decode B=64 H=40 L=8192 d=128",
+            "global_batch": wp.B * world, "seq_len": wp.N, "parallelism": f"replicas x{world}",
+            "l2": "flushed before every step (256 MB write, outside the event-timed launches); "
+                  "decode KV cache 10.7 GB > L2",
+            "prefill_ms": t_pre / K, "decode_ms": t_dec / K, "decode_splits": splits,
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": "fwd_tc_kernel<128>",
+            "achieved": prefill_flops(wp) / pre_launch_s / 1e12, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": prefill_flops(wp) / pre_launch_s / 1e12 / peaks["bf16_tflops"],
+            "peak_source": f"bf16 dense burst, {peaks['source']}",
+            "traffic": traffic.get("fwd_tc_kernel"),
+        },
+        "decode": {
+            "value": dec_gbs, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": decode_bytes(wd) / dec_launch_s / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": decode_bytes(wd) / dec_launch_s / 1e9 / peaks["hbm_gbs"],
+                         "frac_of_8tbs": decode_bytes(wd) / dec_launch_s / 1e9 / 8000.0,
+                         "peak_source": f"HBM copy, {peaks['source']}",
+                         "traffic": traffic.get("decode_kernel")},
+            "e2e": e2e_dec,
+        },
+        "underflow": underflow,
+        "e2e": e2e,
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def load_traffic() -> dict:
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

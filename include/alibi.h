@@ -1,0 +1,144 @@
+/*
+ * alibi.h - C ABI of the GB300 (sm_103a) ALiBi causal attention library.
+ *
+ * Operation (all entry points):
+ *   O = softmax( Q K^T / sqrt(d) - m_h * (i - j), causal mask ) V
+ * with the per-head slope m_h of the ALiBi schedule. Sources (page title,
+ * then section / equation):
+ *   - "When Attention Goes Blind: Numerical Failure in ALiBi Positional
+ *     Encodings" (arXiv 2608.03994), sec. 3.1 eq. 1-3: A = QK^T / sqrt(d_k),
+ *     B = -m D, D = i - j.
+ *   - "ALiBi: Attention with Linear Biases" (abhik.ai): "From distance to a
+ *     normalized weight" (keys j <= i allowed, future keys masked);
+ *     "Different heads, different distance penalties" (slope schedule); the
+ *     KV-cache paragraph after the full-sequence example (true positions).
+ *
+ * Conventions shared by every call:
+ *   - Tensors are dense, row-major and contiguous. Prefill: q, k, v, out are
+ *     [B, H, N, d]; lse is [B, H, N]. Decode: q and out are [B, H, d]; the
+ *     caches are [B, H, L, d].
+ *   - bf16 means IEEE-style bfloat16 (1-8-7), stored as 16-bit words.
+ *   - Device pointers must be CUDA device (or managed) memory of the current
+ *     device, 16-byte aligned. The caller owns every buffer; the library never
+ *     frees or retains a caller pointer after the call returns.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous: results are valid once the stream has been synchronised.
+ *   - scale is 1/sqrt(d); slopes are always those of alibi_slopes(H).
+ *   - Return value: ALIBI_OK, or a negative alibi_status. Argument errors are
+ *     detected on the host before anything is launched. No call aborts the
+ *     process, traps on the device or waits without bound: every device-side
+ *     wait has a time limit, after which the kernel records ALIBI_ERR_TIMEOUT
+ *     in a device status word and returns; alibi_check_error() reports it.
+ */
+#ifndef ALIBI_H
+#define ALIBI_H
+
+#if defined(__GNUC__) || defined(__clang__)
+#define ALIBI_API __attribute__((visibility("default")))
+#else
+#define ALIBI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ALIBI_OK = 0,
+    ALIBI_ERR_INVALID = -1,     /* null pointer, non-positive size, misaligned pointer */
+    ALIBI_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (e.g. d) */
+    ALIBI_ERR_CUDA = -3,        /* a CUDA runtime/driver call or kernel launch failed    */
+    ALIBI_ERR_TIMEOUT = -4      /* a bounded device-side wait expired (see alibi_check_error) */
+} alibi_status;
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+ALIBI_API int alibi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+ALIBI_API const char *alibi_status_str(int status);
+
+/*
+ * ALiBi slopes for H heads, written to HOST memory out_host[0..H-1] as fp32.
+ * "ALiBi: Attention with Linear Biases", "Different heads, different distance
+ * penalties": for a power-of-two H, m_h = 2^(-8(h+1)/H); otherwise the
+ * schedule of the largest power of two c < H followed by every other entry
+ * (1st, 3rd, ...) of the 2c schedule, H - c of them. Each value is the exact
+ * real rounded once to fp32 (round to nearest even). Host-only; H in [1, 4096].
+ */
+ALIBI_API int alibi_slopes(int H, float *out_host);
+
+/*
+ * Causal prefill, bf16 in / bf16 out, fp32 LSE (natural log).
+ * q, k, v: device bf16 [B, H, N, d]; out: device bf16 [B, H, N, d];
+ * lse: device fp32 [B, H, N] (may be NULL to skip it);
+ * LSE_i = ln sum_{j<=i} exp(q_i.k_j/sqrt(d) - m_h (i - j)).
+ * d in {64, 128}; N >= 1; causal must be 1 (0 returns ALIBI_ERR_UNSUPPORTED).
+ * Runs the tcgen05/TMEM/TMA kernel: scores and P.V on the tensor cores with
+ * fp32 accumulation; the bias is generated from tile coordinates and never
+ * stored; online softmax in fp32; P rounded to bf16 for the P.V product.
+ */
+ALIBI_API int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                   int B, int H, int N, int d, int causal, void *stream);
+
+/*
+ * Causal prefill in fp32 (reference precision): all inputs, outputs and
+ * arithmetic in fp32 on the CUDA cores with IEEE expf. Same layouts and
+ * semantics as alibi_attn_fwd; d in [1, 256]; lse may be NULL.
+ */
+ALIBI_API int alibi_attn_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                       int B, int H, int N, int d, int causal, void *stream);
+
+/*
+ * Decode: one new query per (b, h) at its true sequence position L - 1,
+ * attending to keys 0..L-1 of the cache ("ALiBi: Attention with Linear
+ * Biases", KV-cache paragraph): s_j = q.k_j/sqrt(d) - m_h (L - 1 - j).
+ * q: device bf16 [B, H, d]; kcache, vcache: device bf16 [B, H, L, d];
+ * out: device bf16 [B, H, d]. d == 128; L >= 1.
+ * Split-K over the cache with an fp32 partial-softmax merge. When it splits,
+ * the partials buffer is taken from a library-owned stream-ordered memory pool
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).
+ */
+ALIBI_API int alibi_attn_decode(const void *q, const void *kcache, const void *vcache, void *out,
+                      int B, int H, int L, int d, void *stream);
+
+/*
+ * Number of KV-cache splits alibi_attn_decode uses for this shape (host-only,
+ * deterministic for a given device). 1 means a single kernel with no partials
+ * buffer; S > 1 means a split kernel plus a merge kernel and a partials buffer
+ * of B*H*S*(d+4) floats. Returns a negative alibi_status on invalid arguments.
+ */
+ALIBI_API int alibi_attn_decode_splits(int B, int H, int L, int d);
+
+/*
+ * Attention weights of the fp32 path (test and analysis export):
+ * P[b,h,i,j] = exp(q_i.k_j/sqrt(d) - m_h (i - j) - lse[b,h,i]) for j <= i,
+ * 0 for j > i. q, k: device fp32 [B, H, N, d]; lse: device fp32 [B, H, N]
+ * from alibi_attn_fwd_f32; P: device fp32 [B, H, N, N]. d in [1, 256].
+ */
+ALIBI_API int alibi_attn_probs_f32(const float *q, const float *k, const float *lse, float *P,
+                         int B, int H, int N, int d, void *stream);
+
+/*
+ * Underflow count ("When Attention Goes Blind", sec. 3.2-3.3): per head h,
+ * the number of causal pairs (b, i, j <= i) whose max-subtracted exponent
+ * x_ij - M_i (natural-log units, x_ij = q_i.k_j/sqrt(d) - m_h (i - j),
+ * M_i = max_j x_ij) is <= tau. Two passes per row in fp32 (row max, then
+ * count). q, k: device bf16 [B, H, N, d]; counts: device uint64 [H],
+ * overwritten (zeroed on `stream` first). d in {64, 128}.
+ */
+ALIBI_API int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N, int d, float tau,
+                              unsigned long long *counts, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word of the
+ * current device. Returns ALIBI_ERR_TIMEOUT if a kernel gave up a bounded
+ * wait since the last check, ALIBI_ERR_CUDA if the stream reports an error,
+ * else ALIBI_OK.
+ */
+ALIBI_API int alibi_check_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ALIBI_H */

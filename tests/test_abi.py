@@ -1,0 +1,118 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and its
+host-only paths (slopes, argument validation) behave. No device work here."""
+import ctypes
+import os
+import re
+
+import mpmath
+import numpy as np
+import pytest
+
+import alibi_positional_bias_gb300 as ab
+import oracle
+from alibi_positional_bias_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ab.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(alibi_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for n in ["alibi_slopes", "alibi_attn_fwd", "alibi_attn_decode", "alibi_attn_fwd_f32",
+              "alibi_attn_probs_f32", "alibi_attn_underflow_bf16", "alibi_status_str", "alibi_check_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n, ok in ab.exported_symbols(declared_symbols()).items() if not ok]
+    assert not missing, missing
+
+
+def test_library_exports_nothing_undeclared(lib):
+    # visibility is hidden by default: only the extern "C" ABI is exported
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", ab.lib_path()], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("alibi_")}
+    assert exported == set(declared_symbols())
+
+
+def test_version_and_status_strings(lib):
+    assert ab.alibi_version() >= 100
+    for s in (0, -1, -2, -3, -4):
+        assert ab.alibi_status_str(s).startswith("ALIBI_")
+
+
+def test_slopes_match_printed_tables(lib):
+    # "ALiBi: Attention with Linear Biases", slope tables for 4, 8 and 6 heads.
+    assert list(ab.alibi_slopes(4)) == [0.25, 0.0625, 0.015625, 0.00390625]
+    assert list(ab.alibi_slopes(8)) == [0.5, 0.25, 0.125, 0.0625, 0.03125, 0.015625, 0.0078125, 0.00390625]
+    assert list(ab.alibi_slopes(6)) == [0.25, 0.0625, 0.015625, 0.00390625, 0.5, 0.125]
+
+
+def test_slopes_bit_exact_vs_oracle_all_h(lib):
+    for H in range(1, 1025):
+        assert np.array_equal(ab.alibi_slopes(H).view(np.uint32), oracle.slopes_f32(H).view(np.uint32)), H
+
+
+def test_slopes_correctly_rounded_large_h(lib):
+    mpmath.mp.prec = 200
+    for H in (257, 300, 1000, 2047, 4096):
+        got = ab.alibi_slopes(H)
+        for h in range(0, H, max(1, H // 97)):
+            num, den = oracle.slope_exponent(H, h)
+            exact = mpmath.power(2, mpmath.mpf(-num) / den)  # at 200 bits
+            with mpmath.workprec(24):
+                want = float(+exact)
+            assert float(got[h]) == want, (H, h)
+
+
+def test_slopes_rejects_bad_h(lib):
+    buf = (ctypes.c_float * 4)()
+    assert lib.alibi_slopes(0, buf) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_slopes(-3, buf) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_slopes(4, None) == ab.ALIBI_ERR_INVALID
+
+
+# Argument validation happens on the host before any CUDA call, so these run
+# without a GPU. The fake pointer values are never dereferenced.
+P = ctypes.c_void_p(0x10000)
+MIS = ctypes.c_void_p(0x10008)  # not 16-byte aligned
+
+
+def test_fwd_argument_errors(lib):
+    f = lib.alibi_attn_fwd
+    assert f(None, P, P, P, P, 1, 1, 8, 64, 1, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, 0, 1, 8, 64, 1, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, 1, 1, 0, 64, 1, None) == ab.ALIBI_ERR_INVALID
+    assert f(MIS, P, P, P, P, 1, 1, 8, 64, 1, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, 1, 1, 8, 64, 2, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, 1, 1, 8, 64, 0, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, 1, 1, 8, 32, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, 1, 300, 8, 64, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
+
+
+def test_decode_and_aux_argument_errors(lib):
+    assert lib.alibi_attn_decode(None, P, P, P, 1, 1, 8, 128, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 0, 128, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 8, 64, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_fwd_f32(P, P, P, P, P, 1, 1, 8, 512, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_probs_f32(P, P, None, P, 1, 1, 8, 16, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_underflow_bf16(P, P, 1, 1, 8, 48, ctypes.c_float(-87.0), P, None) == \
+        ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_underflow_bf16(P, P, 1, 1, 8, 64, ctypes.c_float(float("nan")), P, None) == \
+        ab.ALIBI_ERR_INVALID

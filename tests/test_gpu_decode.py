@@ -1,0 +1,64 @@
+"""bf16 split-K decode vs the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+
+import alibi_inputs as gen
+import oracle
+from gpu_helpers import assert_bf16_out, dev, host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ab():
+    import alibi_positional_bias_gb300 as ab
+    ab.load()
+    return ab
+
+
+@pytest.mark.parametrize("B,H,L", [(1, 1, 1), (1, 3, 5), (2, 2, 16), (1, 2, 17), (1, 4, 100), (2, 3, 513),
+                                   (1, 1, 1000), (3, 5, 4097), (1, 2, 20000), (4, 40, 300)])
+def test_decode_sweep(ab, B, H, L):
+    w = gen.Workload("dec", "decode", B, H, L, 128, "bf16", seed=11 + L)
+    q, k, v = gen.generate(w)
+    out = ab.alibi_attn_decode(dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16"))
+    ab.alibi_check_error()
+    ro, _ = oracle.decode(q.f32, k.f32, v.f32)
+    assert_bf16_out(host64(out), ro)
+
+
+def test_decode_matches_prefill_last_row(ab):
+    # decode at position L-1 sees what prefill row L-1 sees (same kernel family, same inputs)
+    B, H, L = 1, 4, 777
+    q, k, v = gen.random_case(21, B, H, L, 128, dtype="bf16")
+    qd = gen.make_tensor(q.f32[:, :, L - 1, :], (B, H, 128), "bf16")
+    out = ab.alibi_attn_decode(dev(qd, "bf16"), dev(k, "bf16"), dev(v, "bf16"))
+    ab.alibi_check_error()
+    ro, _, _ = oracle.attention(q.f32, k.f32, v.f32, rows=[h * L + L - 1 for h in range(H)])
+    assert_bf16_out(host64(out).reshape(H, 128), ro)
+
+
+def test_decode_full_size_sampled_heads(ab):
+    # B=64 sequences, H=40 (32-head schedule + alternating 64-head entries),
+    # L=8192, d=128: the benchmark's launch; the oracle checks sampled (b, h).
+    import torch
+    w = gen.WORKLOADS["decode_l8192"]
+    qs, ks, _ = w.shapes()
+    qd = torch.empty(qs, dtype=torch.bfloat16, device="cuda")
+    kd = torch.empty(ks, dtype=torch.bfloat16, device="cuda")
+    vd = torch.empty(ks, dtype=torch.bfloat16, device="cuda")
+    for i, t in enumerate((qd, kd, vd)):
+        gen.fill_device(w, i, t)
+    out = host64(ab.alibi_attn_decode(qd, kd, vd))
+    ab.alibi_check_error()
+    assert np.isfinite(out).all()
+    m = oracle.slopes(w.H)
+    rng = np.random.default_rng(0)
+    picks = [(0, 0), (63, 39), (5, 32), (17, 39)] + [(int(b), int(h)) for b, h in
+                                                     zip(rng.integers(0, 64, 20), rng.integers(0, 40, 20))]
+    for b, h in picks:
+        qh = gen.head_slice(w, 0, b, h)
+        kh = gen.head_slice(w, 1, b, h)
+        vh = gen.head_slice(w, 2, b, h)
+        ro, _ = oracle.decode(qh.f32[None, None], kh.f32[None, None], vh.f32[None, None], m=m[h:h + 1])
+        assert_bf16_out(out[b, h], ro[0, 0], what=f"out[{b},{h}]")

@@ -1,0 +1,98 @@
+"""bf16 tcgen05 prefill vs the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+
+import alibi_inputs as gen
+import oracle
+from gpu_helpers import TOL_BF16_LSE, assert_bf16_out, assert_close, dev, host64, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ab():
+    import alibi_positional_bias_gb300 as ab
+    ab.load()
+    return ab
+
+
+def run_bf16(ab, q, k, v):
+    qd, kd, vd = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    out, lse = ab.alibi_attn_fwd(qd, kd, vd)
+    ab.alibi_check_error()
+    return host64(out), host64(lse)
+
+
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 1, 1, 64), (1, 2, 7, 128), (1, 1, 64, 64), (1, 3, 127, 128), (2, 2, 128, 64), (1, 2, 129, 128),
+    (1, 1, 255, 64), (1, 2, 256, 128), (1, 1, 257, 128), (1, 3, 383, 64), (2, 3, 1000, 64), (1, 4, 700, 128),
+    (1, 1, 1537, 128),
+])
+def test_prefill_shape_sweep(ab, B, H, N, d):
+    q, k, v = gen.random_case(7 + N + d + H, B, H, N, d, dtype="bf16")
+    out, lse = run_bf16(ab, q, k, v)
+    ro, rl, _ = oracle.attention(q.f32, k.f32, v.f32)
+    assert_bf16_out(out, ro)
+    assert_close(lse, rl, TOL_BF16_LSE, "lse")
+
+
+def test_heads6_n1024_full(ab):
+    # B=2, H=6 (non-power-of-two slopes), N=1024, d=64, bf16 N(0, 1): every row
+    q, k, v = gen.generate(gen.WORKLOADS["heads6_n1024"])
+    out, lse = run_bf16(ab, q, k, v)
+    ro, rl, _ = oracle.attention(q.f32, k.f32, v.f32)
+    assert_bf16_out(out, ro)
+    assert_close(lse, rl, TOL_BF16_LSE, "lse")
+
+
+@pytest.mark.parametrize("name", ["layer_n2048", "long_n16384"])
+def test_full_size_sampled_rows(ab, name):
+    # the full-size workloads, in the launch configuration the benchmark times;
+    # the oracle checks sampled rows (tile edges, ragged tail, random)
+    w = gen.WORKLOADS[name]
+    q, k, v = gen.generate(w)
+    out, lse = run_bf16(ab, q, k, v)
+    rows = sample_rows(w.B, w.H, w.N, max_heads=8, per_head=16)
+    ro, rl, _ = oracle.attention(q.f32, k.f32, v.f32, rows=rows)
+    assert_bf16_out(out.reshape(-1, w.d)[rows], ro)
+    assert_close(lse.reshape(-1)[rows], rl, TOL_BF16_LSE, "lse")
+    # properties at every row: finite, outputs inside the convex hull of V's range
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    vmax = np.abs(v.f32).max()
+    assert np.abs(out).max() <= vmax * (1 + 2 ** -8)
+
+
+def test_repeatable_and_lse_optional(ab):
+    import torch
+    q, k, v = gen.random_case(3, 1, 2, 300, 128, dtype="bf16")
+    qd, kd, vd = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    o1, l1 = ab.alibi_attn_fwd(qd, kd, vd)
+    o2, l2 = ab.alibi_attn_fwd(qd, kd, vd)
+    o3, l3 = ab.alibi_attn_fwd(qd, kd, vd, want_lse=False)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o4, _ = ab.alibi_attn_fwd(qd, kd, vd)
+    s.synchronize()
+    ab.alibi_check_error()
+    assert l3 is None
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3) and torch.equal(o1, o4)
+
+
+def test_equal_scores_recency_on_gpu(ab):
+    # identical K rows: each row's weights fall by e^{-m} per token of distance
+    # ("ALiBi: Attention with Linear Biases", "From distance to a normalized
+    # weight"); with V = one-hot positions the output exposes the weights.
+    import torch
+    H, N, d = 4, 128, 128
+    rng = np.random.default_rng(5)
+    q = gen.make_tensor(rng.standard_normal((1, H, N, d)), (1, H, N, d), "bf16")
+    k = gen.make_tensor(np.broadcast_to(rng.standard_normal(d), (1, H, N, d)), (1, H, N, d), "bf16")
+    v = gen.make_tensor(np.broadcast_to(np.eye(N, d), (1, H, N, d)), (1, H, N, d), "bf16")
+    out, lse = run_bf16(ab, q, k, v)
+    m = oracle.slopes(H)
+    for h in range(H):
+        i = N - 1
+        w = out[0, h, i, : i + 1]
+        want = np.exp(-m[h] * (i - np.arange(i + 1)))
+        want /= want.sum()
+        assert np.abs(w - want).max() <= 1e-2 * max(1.0, want.max())
