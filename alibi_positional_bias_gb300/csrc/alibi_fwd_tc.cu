@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int j = t.n - 1 - it;
                 ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_SM_S);
                 ++s_cnt;
+                ok = __all_sync(0xffffffffu, ok);  // keep the warp converged for tcgen05.ld
                 if (!ok) break;
                 tc_fence_after();
                 float x[BN];
@@ -326,13 +327,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         mt = fmaxf(mt, x[c]);
                     }
                 }
-                if (it == it0) {
-                    M = mt;
-                } else if (mt > M + kRescaleThreshold) {
-                    // raise the running max; O_s is quiescent: S_s(it) completing implies PV_s(it-1) did
-                    const float alpha = ex2_approx(M - mt);
-                    M = mt;
-                    l *= alpha;
+                // Raise the running max lazily: only when this tile exceeds it by 2^8. The
+                // decision is per row, but tcgen05.ld/st are warp-collective (.sync.aligned),
+                // so the warp rescales together when any of its rows needs it and rows that
+                // do not use alpha = 1. O_s is quiescent here: S_s(it) completing implies
+                // PV_s(it-1), issued before it, has completed.
+                const bool need = (it != it0) && (mt > M + kRescaleThreshold);
+                if (it == it0) M = mt;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ex2_approx(M - mt) : 1.0f;
+                    if (need) {
+                        M = mt;
+                        l *= alpha;
+                    }
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -363,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             // ------------------------------------------------------ epilogue
             ok = mbar_wait(&o_full[s], o_cnt & 1, err, SITE_SM_O);
             ++o_cnt;
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             const float inv_l = 1.0f / l;

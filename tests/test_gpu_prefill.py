@@ -96,3 +96,24 @@ def test_equal_scores_recency_on_gpu(ab):
         want = np.exp(-m[h] * (i - np.arange(i + 1)))
         want /= want.sum()
         assert np.abs(w - want).max() <= 1e-2 * max(1.0, want.max())
+
+
+def test_lazy_rescale_with_divergent_rows(ab):
+    # Rows of one warp disagree on raising the running max: even rows meet low
+    # scores on their diagonal tile and high scores one tile back, odd rows the
+    # reverse. Scores reach +-sigma |u|^2 / sqrt(d) with sigma = 40, well past
+    # the 2^8 lazy-rescale threshold.
+    H, N, d = 1, 384, 128
+    rng = np.random.default_rng(8)
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    sign_q = np.where(np.arange(N) % 2 == 0, 1.0, -1.0)
+    q = 40.0 * sign_q[:, None] * u[None, :] + 0.1 * rng.standard_normal((N, d))
+    tile = np.arange(N) // 128
+    k = np.where((tile % 2 == 0)[:, None], 1.0, -1.0) * u[None, :] * 6.0 + 0.1 * rng.standard_normal((N, d))
+    v = rng.standard_normal((N, d))
+    qt, kt, vt = (gen.make_tensor(x[None, None], (1, H, N, d), "bf16") for x in (q, k, v))
+    out, lse = run_bf16(ab, qt, kt, vt)
+    ro, rl, _ = oracle.attention(qt.f32, kt.f32, vt.f32)
+    assert_bf16_out(out, ro)
+    assert_close(lse, rl, TOL_BF16_LSE, "lse")
