@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
     "alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
-    "alibi_attn_underflow_bf16", "alibi_check_error",
+    "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc",
 ]
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
@@ -62,6 +62,8 @@ def load(build_if_missing: bool = False):
         lib.alibi_attn_decode.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
         lib.alibi_attn_probs_f32.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
         lib.alibi_attn_decode_splits.argtypes = [I, I, I, I]
+        lib.alibi_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
+        lib.alibi_attn_decode_noalloc.restype = I
         lib.alibi_attn_underflow_bf16.argtypes = [vp, vp, I, I, I, I, F, vp, vp]
         lib.alibi_check_error.argtypes = [vp]
         for name in ("alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits",
@@ -179,6 +181,24 @@ def alibi_attn_decode(q, kcache, vcache, out=None, stream=None):
     _need(out, torch.bfloat16, (B, H, d), "out")
     _check(load().alibi_attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, L, d,
                                     _stream(stream, q.device)), "alibi_attn_decode")
+    return out
+
+
+def alibi_attn_decode_noalloc(q, kcache, vcache, out, stream=None):
+    """Decode without any device allocation (for callers that cannot allocate).
+
+    Same result as alibi_attn_decode, but the split-K partials live in a fixed
+    4 MiB buffer inside the library, so ``out`` must be supplied by the caller.
+    Calls that overlap on the GPU share that buffer and race: order them.
+    """
+    import torch
+    _need(kcache, torch.bfloat16, None, "kcache")
+    B, H, L, d = kcache.shape
+    _need(vcache, torch.bfloat16, kcache.shape, "vcache")
+    _need(q, torch.bfloat16, (B, H, d), "q")
+    _need(out, torch.bfloat16, (B, H, d), "out")
+    _check(load().alibi_attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, L, d,
+                                            _stream(stream, q.device)), "alibi_attn_decode_noalloc")
     return out
 
 

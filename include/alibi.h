@@ -110,6 +110,27 @@ ALIBI_API int alibi_attn_decode(const void *q, const void *kcache, const void *v
 ALIBI_API int alibi_attn_decode_splits(int B, int H, int L, int d);
 
 /*
+ * Decode that allocates nothing. The pages have no counterpart to this entry
+ * point: it is for callers that cannot let a library allocate device memory
+ * (a serving process whose allocator already reserved the whole GPU, a
+ * real-time decode loop that cannot absorb allocation latency, a runtime that
+ * forbids allocations outside its own arena). Same arguments, layouts, split
+ * plan and results as alibi_attn_decode; the caller still passes inputs and
+ * outputs. The split-K partials live in a fixed 4 MiB device buffer compiled
+ * into the library (held by every GPU that loads it until process exit); no
+ * cudaMalloc, cudaFree or pool allocation happens.
+ *   - The first call on each device does a one-time set-up (it looks up the
+ *     buffer's device address); make that first call before any stream capture.
+ *   - All calls share the buffer and it keeps the last call's contents (each
+ *     call overwrites every partial it reads, so nothing needs clearing). Calls
+ *     that overlap on the GPU (e.g. on different streams) race on it: order them.
+ *   - Returns ALIBI_ERR_UNSUPPORTED if the split plan needs more than 4 MiB of
+ *     partials (B*H*S*(d+4)*4 bytes with S = alibi_attn_decode_splits(...)).
+ */
+ALIBI_API int alibi_attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, void *out,
+                      int B, int H, int L, int d, void *stream);
+
+/*
  * Attention weights of the fp32 path (test and analysis export):
  * P[b,h,i,j] = exp(q_i.k_j/sqrt(d) - m_h (i - j) - lse[b,h,i]) for j <= i,
  * 0 for j > i. q, k: device fp32 [B, H, N, d]; lse: device fp32 [B, H, N]
