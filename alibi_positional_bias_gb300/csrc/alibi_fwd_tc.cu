@@ -41,6 +41,13 @@ constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Register split: the kernel launches with kLaunchRegs per thread (384 threads,
+// one CTA per SM); the producer/MMA warpgroup gives registers back and the two
+// softmax warpgroups take them. The shares add up exactly to the launch total.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kRegsLow = 88;    // warps 0-3
+constexpr uint32_t kRegsHigh = 208;  // warps 4-11
+static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split must match launch");
 
 template <int D>
 struct Cfg {
@@ -74,6 +81,27 @@ struct Item {
     int bh, qb, n;
     bool q1valid;
 };
+
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Max of 128 values as 8 independent chains of three-input max (short dependency chains).
+__device__ __forceinline__ float row_max128(const float (&x)[128])
+{
+    float m[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m[k] = x[k];
+#pragma unroll
+        for (int t = 1; t + 1 < 16; t += 2) m[k] = max3f(m[k], x[k + 8 * t], x[k + 8 * (t + 1)]);
+        m[k] = fmaxf(m[k], x[k + 8 * 15]);
+    }
+    return fmaxf(max3f(m[0], m[1], m[2]), max3f(max3f(m[3], m[4], m[5]), m[6], m[7]));
+}
 
 __device__ __forceinline__ int item_index(int k)
 {
@@ -151,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) {
+    // producer / MMA warpgroup: give registers back (all four warps execute this)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -280,8 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, err, SITE_MMA_DONE);
         }
-    } else if (warp >= 4) {
+    }
+    } else {
         // ------------------------------------------------ softmax warpgroups
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         const int s = (warp - 4) >> 2;
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;
@@ -305,28 +338,31 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 ok = __all_sync(0xffffffffu, ok);  // keep the warp converged for tcgen05.ld
                 if (!ok) break;
                 tc_fence_after();
-                float x[BN];
+                uint32_t sraw[BN];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c)
-                    tmem_ld32(lane_addr + s * 128 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+                    tmem_ld32(lane_addr + s * 128 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sraw[c * 32]));
                 tmem_wait_ld();
-                // x = s * log2(e)/sqrt(d) - m log2(e) (i - j), from the integer offset i - k0
+                // x = s log2(e)/sqrt(d) - m log2(e) (i - j): the bias of key k0 + c is
+                // nb + sl2 c with nb = -sl2 (i - k0) from the integer offset, so no large
+                // absolute position enters the fp32 arithmetic.
                 const float nb = -sl2 * static_cast<float>(i - j * BN);
-                float mt = -INFINITY;
-                if (j == qt) {
+                const float2 c1v = make_float2(p.c1, p.c1);
+                float x[BN];
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        const float b = fmaf(sl2, static_cast<float>(c), nb);
-                        x[c] = (c > r) ? -INFINITY : fmaf(x[c], p.c1, b);
-                        mt = fmaxf(mt, x[c]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        x[c] = fmaf(x[c], p.c1, fmaf(sl2, static_cast<float>(c), nb));
-                        mt = fmaxf(mt, x[c]);
-                    }
+                for (int u = 0; u < BN / 2; ++u) {
+                    const float2 b = make_float2(fmaf(sl2, static_cast<float>(2 * u), nb),
+                                                 fmaf(sl2, static_cast<float>(2 * u + 1), nb));
+                    const float2 xv =
+                        __ffma2_rn(make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, b);
+                    x[2 * u] = xv.x;
+                    x[2 * u + 1] = xv.y;
                 }
+                if (j == qt) {  // diagonal tile: keys after the query are masked
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) x[c] = (c > r) ? -INFINITY : x[c];
+                }
+                const float mt = row_max128(x);
                 // Raise the running max lazily: only when this tile exceeds it by 2^8. The
                 // decision is per row, but tcgen05.ld/st are warp-collective (.sync.aligned),
                 // so the warp rescales together when any of its rows needs it and rows that
@@ -350,16 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_st32(lane_addr + 256 + s * 128 + c * 32, o);
                     }
                 }
-                float sum = 0.f;
+                // p = 2^(x - M), packed to bf16 pairs; four independent pair sums
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                const float2 negM = make_float2(-M, -M);
                 uint32_t pk[BN / 2];
 #pragma unroll
                 for (int u = 0; u < BN / 2; ++u) {
-                    const float p0 = ex2_approx(x[2 * u] - M);
-                    const float p1 = ex2_approx(x[2 * u + 1] - M);
-                    sum += p0 + p1;
-                    pk[u] = pack_bf16x2(p0, p1);
+                    const float2 dv = __fadd2_rn(make_float2(x[2 * u], x[2 * u + 1]), negM);
+                    const float2 pv = make_float2(ex2_approx(dv.x), ex2_approx(dv.y));
+                    acc[u & 3] = __fadd2_rn(acc[u & 3], pv);
+                    pk[u] = pack_bf16x2(pv.x, pv.y);
                 }
-                l += sum;
+                const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+                const float2 a = __fadd2_rn(a01, a23);
+                l += a.x + a.y;
                 tmem_st32(lane_addr + s * 128, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
                 tmem_st32(lane_addr + s * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
                 tmem_wait_st();
@@ -432,7 +473,14 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
 
     static bool attr_set = false;  // per process; the attribute is per function
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        // The register split above only balances if the kernel launches with exactly
+        // kLaunchRegs per thread; refuse to launch otherwise (an unbalanced
+        // setmaxnreg.inc would wait for registers that never come).
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
