@@ -159,9 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
             mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 128);
+            mbar_init(&p_full[s], 4);   // one arrival per softmax warp
             mbar_init(&o_full[s], 1);
-            mbar_init(&o_empty[s], 128);
+            mbar_init(&o_empty[s], 4);
         }
         mbar_init(q_empty, 1);
         mbar_init(mma_done, 1);
@@ -238,24 +238,29 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
 
-                // S_s = Q_s K^T over d in steps of 16 (K-major operands, 32-byte steps inside a swizzle atom)
+                // S_s = Q_s K^T over d in steps of 16 (K-major operands, 32-byte steps inside a
+                // swizzle atom, 16 KB per 64-column atom). Descriptors are built once per tile;
+                // each step adds a compile-time offset to the 14-bit address field (smem
+                // addresses stay below 256 KB, so the field never carries).
                 auto issue_S = [&](int s, uint32_t kst) {
-                    const uint32_t qa = sQ + s * C::kTileBytes, kb = sK + kst * C::kTileBytes;
+                    const uint64_t qd = smem_desc_sw128(sQ + s * C::kTileBytes, 16, 1024);
+                    const uint64_t kd = smem_desc_sw128(sK + kst * C::kTileBytes, 16, 1024);
+                    const uint32_t dst = tmem + s * 128;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                        mma_ss(tmem + s * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                               idS, kk > 0);
+                        const uint32_t step = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                        mma_ss(dst, qd + step, kd + step, idS, kk > 0);
                     }
                     mma_commit(&s_full[s]);
                 };
-                // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous)
+                // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous;
+                // 16 keys = 2048 bytes per step)
                 auto issue_PV = [&](int s, uint32_t vst, bool first) {
-                    const uint32_t vb = sV + vst * C::kTileBytes;
+                    const uint64_t vd = smem_desc_sw128(sV + vst * C::kTileBytes, C::kChunkBytes, 1024);
+                    const uint32_t dst = tmem + 256 + s * 128, pa = tmem + s * 128;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ts(tmem + 256 + s * 128, tmem + s * 128 + kk * 8,
-                               smem_desc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), idO, (first && kk == 0) ? 0u : 1u);
+                        mma_ts(dst, pa + kk * 8, vd + ((kk * 2048) >> 4), idO, (first && kk == 0) ? 0u : 1u);
                 };
 
                 bool first_pv[2] = {true, true};
@@ -405,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 tmem_st32(lane_addr + s * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&p_full[s]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[s]);
             }
             if (!ok) break;
             // ------------------------------------------------------ epilogue
@@ -433,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
             }
             tc_fence_before();
-            mbar_arrive(&o_empty[s]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[s]);
             if (valid && p.lse) p.lse[static_cast<size_t>(t.bh) * p.N + i] = (M + __log2f(l)) * 0.69314718055994531f;
         }
     }

@@ -68,20 +68,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait until the phase with the given parity has completed, for at most
-// kWaitLimitNs. Returns false (and records ALIBI_DEV_TIMEOUT) on expiry, or
-// immediately if another thread already recorded an error.
+// about kWaitLimitNs. Returns false (and records ALIBI_DEV_TIMEOUT) on expiry,
+// or early if another thread already recorded an error. The error word (a
+// global load) and the global timer are read only every 256 polls, so a
+// completed phase is noticed without an L2 round trip on the critical path.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t site)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    uint64_t t0 = 0;
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*(volatile uint32_t *)err != 0u) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            report_error(err, ALIBI_DEV_TIMEOUT, site);
-            return false;
+    for (uint32_t n = 0;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 255u) == 255u) {
+            if (*(volatile uint32_t *)err != 0u) return false;
+            const uint64_t t = global_timer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kWaitLimitNs) {
+                report_error(err, ALIBI_DEV_TIMEOUT, site);
+                return false;
+            }
         }
     }
 }
