@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     uint64_t *o_full = bars + 15;   // [2]
     uint64_t *o_empty = bars + 17;  // [2]
     uint64_t *mma_done = bars + 19; // [1]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+    uint64_t *p_hi = bars + 20;     // [2] P of keys 64..127 written (p_full covers keys 0..63)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 22);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(&v_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 4);   // one arrival per softmax warp
+            mbar_init(&p_hi[s], 4);
             mbar_init(&o_full[s], 1);
             mbar_init(&o_empty[s], 4);
         }
@@ -236,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const int last_slot = t.q1valid ? 1 : 0;
                 ok = mbar_wait(&q_full[0], k & 1, err, SITE_MMA_Q) && mbar_wait(&q_full[1], k & 1, err, SITE_MMA_Q);
                 if (!ok) break;
-                tc_fence_after();
 
                 // S_s = Q_s K^T over d in steps of 16 (K-major operands, 32-byte steps inside a
                 // swizzle atom, 16 KB per 64-column atom). Descriptors are built once per tile;
@@ -255,12 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 };
                 // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous;
                 // 16 keys = 2048 bytes per step)
-                auto issue_PV = [&](int s, uint32_t vst, bool first) {
+                // (issued in two halves of 64 keys as the softmax hands P over)
+                auto issue_PV_half = [&](int s, uint32_t vst, bool first, int half) {
                     const uint64_t vd = smem_desc_sw128(sV + vst * C::kTileBytes, C::kChunkBytes, 1024);
                     const uint32_t dst = tmem + 256 + s * 128, pa = tmem + s * 128;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
+                    for (int k4 = 0; k4 < BN / 32; ++k4) {
+                        const int kk = half * (BN / 32) + k4;
                         mma_ts(dst, pa + kk * 8, vd + ((kk * 2048) >> 4), idO, (first && kk == 0) ? 0u : 1u);
+                    }
                 };
 
                 bool first_pv[2] = {true, true};
@@ -269,25 +273,33 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const uint32_t st = kc % 2, ph = (kc / 2) & 1;
                     ok = mbar_wait(&k_full[st], ph, err, SITE_MMA_K);
                     if (!ok) break;
-                    tc_fence_after();
                     for (int s = 0; s < 2; ++s)
                         if (slot_active(t, s, 0)) issue_S(s, st);
                     mma_commit(&k_empty[st]);
                 }
-                int k_ready = 0;  // highest iteration whose K tile has been waited for
                 for (int it = 0; it < t.n && ok; ++it) {
                     const uint32_t vst = (vc + it) % 2, vph = ((vc + it) / 2) & 1;
                     ok = mbar_wait(&v_full[vst], vph, err, SITE_MMA_V);
                     if (!ok) break;
-                    tc_fence_after();
+                    // the next K tile is normally resident long before it is needed: wait
+                    // for it here, off the P -> PV -> S critical path
+                    if (it + 1 < t.n) {
+                        const uint32_t kst = (kc + it + 1) % 2, kph = ((kc + it + 1) / 2) & 1;
+                        ok = mbar_wait(&k_full[kst], kph, err, SITE_MMA_K);
+                        if (!ok) break;
+                    }
                     for (int s = 0; s < 2 && ok; ++s) {
                         if (slot_active(t, s, it)) {
                             ok = mbar_wait(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
-                            ++p_cnt[s];
                             if (ok && first_pv[s]) ok = mbar_wait(&o_empty[s], (o_cnt[s] & 1) ^ 1, err, SITE_MMA_O);
                             if (!ok) break;
                             tc_fence_after();
-                            issue_PV(s, vst, first_pv[s]);
+                            issue_PV_half(s, vst, first_pv[s], 0);
+                            ok = mbar_wait(&p_hi[s], p_cnt[s] & 1, err, SITE_MMA_P);
+                            ++p_cnt[s];
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_PV_half(s, vst, first_pv[s], 1);
                             first_pv[s] = false;
                             if (it == t.n - 1) {
                                 mma_commit(&o_full[s]);
@@ -295,13 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                             }
                         }
                         if (it + 1 < t.n && slot_active(t, s, it + 1)) {
-                            const uint32_t kst = (kc + it + 1) % 2, kph = ((kc + it + 1) / 2) & 1;
-                            if (k_ready < it + 1) {
-                                ok = mbar_wait(&k_full[kst], kph, err, SITE_MMA_K);
-                                if (!ok) break;
-                                tc_fence_after();
-                                k_ready = it + 1;
-                            }
+                            const uint32_t kst = (kc + it + 1) % 2;
                             issue_S(s, kst);
                             if (s == last_slot) mma_commit(&k_empty[kst]);
                         }
@@ -395,23 +401,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
                 const float2 negM = make_float2(-M, -M);
+                // Two halves of 64 keys: the first half of P is handed to the MMA issuer
+                // (p_full) while the second half is still being exponentiated (p_hi).
                 uint32_t pk[BN / 2];
 #pragma unroll
-                for (int u = 0; u < BN / 2; ++u) {
-                    const float2 dv = __fadd2_rn(make_float2(x[2 * u], x[2 * u + 1]), negM);
-                    const float2 pv = make_float2(ex2_approx(dv.x), ex2_approx(dv.y));
-                    acc[u & 3] = __fadd2_rn(acc[u & 3], pv);
-                    pk[u] = pack_bf16x2(pv.x, pv.y);
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int u = half * (BN / 4); u < (half + 1) * (BN / 4); ++u) {
+                        const float2 dv = __fadd2_rn(make_float2(x[2 * u], x[2 * u + 1]), negM);
+                        const float2 pv = make_float2(ex2_approx(dv.x), ex2_approx(dv.y));
+                        acc[u & 3] = __fadd2_rn(acc[u & 3], pv);
+                        pk[u] = pack_bf16x2(pv.x, pv.y);
+                    }
+                    tmem_st32(lane_addr + s * 128 + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[half * 32]));
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(half == 0 ? &p_full[s] : &p_hi[s]);
                 }
                 const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
                 const float2 a = __fadd2_rn(a01, a23);
                 l += a.x + a.y;
-                tmem_st32(lane_addr + s * 128, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-                tmem_st32(lane_addr + s * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[s]);
             }
             if (!ok) break;
             // ------------------------------------------------------ epilogue

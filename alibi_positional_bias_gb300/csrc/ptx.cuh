@@ -72,8 +72,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // or early if another thread already recorded an error. The error word (a
 // global load) and the global timer are read only every 256 polls, so a
 // completed phase is noticed without an L2 round trip on the critical path.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t site)
 {
+    if (mbar_test(bar, parity)) return true;  // already complete: no suspend
     uint64_t t0 = 0;
 #pragma unroll 1
     for (uint32_t n = 0;; ++n) {
