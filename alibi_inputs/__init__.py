@@ -236,16 +236,19 @@ def random_case(seed: int, B: int, H: int, N: int, d: int, dtype: str = "bf16", 
     return generate(w)
 
 
-def fill_device(w: Workload, idx: int, dst, chunk: int = 1 << 27) -> None:
+def fill_device(w: Workload, idx: int, dst, chunk: int = 1 << 27, start: int = 0) -> None:
     """Write tensor idx of workload w into the contiguous torch CUDA tensor ``dst``
-    (bf16 or fp32) chunk by chunk, without materialising it on the host."""
+    (bf16 or fp32) chunk by chunk, without materialising it on the host.
+
+    ``start`` is the flat element offset of ``dst`` inside the workload's tensor
+    (a rank's shard of a global batch is a contiguous slice)."""
     import torch
     total = dst.numel()
-    assert total == int(np.prod(w.shapes()[idx])) and dst.is_contiguous()
+    assert start + total <= int(np.prod(w.shapes()[idx])) and dst.is_contiguous()
     flat = dst.view(-1)
     for s in range(0, total, chunk):
         c = min(chunk, total - s)
-        vals = tensor_values(w, idx, s, c)
+        vals = tensor_values(w, idx, start + s, c)
         if dst.dtype == torch.bfloat16:
             host = torch.from_numpy(f32_to_bf16_bits(vals).view(np.int16)).view(torch.bfloat16)
         else:

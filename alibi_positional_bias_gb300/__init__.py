@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
     "alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
-    "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc",
+    "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc", "alibi_selftest_timeout",
 ]
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
@@ -66,6 +66,8 @@ def load(build_if_missing: bool = False):
         lib.alibi_attn_decode_noalloc.restype = I
         lib.alibi_attn_underflow_bf16.argtypes = [vp, vp, I, I, I, I, F, vp, vp]
         lib.alibi_check_error.argtypes = [vp]
+        lib.alibi_selftest_timeout.argtypes = [vp]
+        lib.alibi_selftest_timeout.restype = I
         for name in ("alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits",
                      "alibi_attn_probs_f32",
                      "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_slopes"):
@@ -237,6 +239,12 @@ def alibi_attn_underflow_bf16(q, k, tau: float, counts=None, stream=None):
     _check(load().alibi_attn_underflow_bf16(_ptr(q), _ptr(k), B, H, N, d, ctypes.c_float(tau), _ptr(counts),
                                             _stream(stream, q.device)), "alibi_attn_underflow_bf16")
     return counts
+
+
+def alibi_selftest_timeout(stream=None) -> None:
+    """Launch the failure-path self-test (a bounded wait that must time out)."""
+    import torch
+    _check(load().alibi_selftest_timeout(_stream(stream, torch.cuda.current_device())), "alibi_selftest_timeout")
 
 
 def alibi_check_error(stream=None, device=None) -> None:

@@ -272,6 +272,11 @@ int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N,
     return to_status(launch_underflow(q, k, B, H, N, d, tau, counts, s, static_cast<cudaStream_t>(stream)));
 }
 
+int alibi_selftest_timeout(void *stream)
+{
+    return to_status(launch_selftest_timeout(static_cast<cudaStream_t>(stream)));
+}
+
 int alibi_check_error(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ALIBI_ERR_CUDA;

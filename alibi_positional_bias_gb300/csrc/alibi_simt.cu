@@ -183,7 +183,27 @@ __global__ void __launch_bounds__(kUfRows) underflow_kernel(const __nv_bfloat16 
     }
 }
 
+// Waits on a barrier nobody arrives on: the bounded wait must give up and record
+// a timeout (failure-path self-test).
+__global__ void selftest_timeout_kernel(uint32_t *err)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait(&bar, 0, err, 0x901);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_timeout(cudaStream_t stream)
+{
+    uint32_t *err = device_status_word();
+    if (!err) return cudaErrorInvalidDevice;
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B, int H,
                            int N, int d, const Slopes &slopes, cudaStream_t stream)

@@ -50,6 +50,7 @@ cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, f
                              int d, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
                           const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(cudaStream_t stream);
 cudaError_t launch_underflow(const void *q, const void *k, int B, int H, int N, int d, float tau,
                              unsigned long long *counts, const Slopes &slopes, cudaStream_t stream);
 

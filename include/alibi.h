@@ -151,6 +151,17 @@ ALIBI_API int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int
                               unsigned long long *counts, void *stream);
 
 /*
+ * Self-test of the failure path; the pages have no counterpart to it. Launches
+ * one CTA whose thread waits on a shared-memory barrier that nothing ever
+ * arrives on, through the same bounded wait every kernel uses. After about one
+ * second the wait gives up, records a timeout in the device status word and the
+ * kernel returns normally; alibi_check_error(stream) then returns
+ * ALIBI_ERR_TIMEOUT and clears the word. No fault, trap or hang is involved and
+ * the CUDA context stays usable.
+ */
+ALIBI_API int alibi_selftest_timeout(void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the device status word of the
  * current device. Returns ALIBI_ERR_TIMEOUT if a kernel gave up a bounded
  * wait since the last check, ALIBI_ERR_CUDA if the stream reports an error,
