@@ -20,11 +20,12 @@ from . import _build
 
 __all__ = [
     "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
-    "alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
+    "alibi_attn_fwd", "alibi_attn_fwd_ex", "alibi_attn_skip_plan", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
     "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc", "alibi_selftest_timeout",
 ]
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
+ALIBI_FWD_SKIP_UNDERFLOW, ALIBI_FWD_CLAMP, ALIBI_FWD_LOGDIST, ALIBI_FWD_SOFTCAP = 1, 2, 4, 8
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +60,10 @@ def load(build_if_missing: bool = False):
         lib.alibi_slopes.argtypes = [I, ctypes.POINTER(F)]
         lib.alibi_attn_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
+        lib.alibi_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, ctypes.c_uint, F, F, vp]
+        lib.alibi_attn_fwd_ex.restype = I
+        lib.alibi_attn_skip_plan.argtypes = [vp, vp, I, I, I, I, vp, vp]
+        lib.alibi_attn_skip_plan.restype = I
         lib.alibi_attn_decode.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
         lib.alibi_attn_probs_f32.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
         lib.alibi_attn_decode_splits.argtypes = [I, I, I, I]
@@ -134,8 +139,13 @@ def alibi_slopes(H: int) -> np.ndarray:
     return out
 
 
-def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None, want_lse: bool = True):
-    """bf16 causal prefill on the tensor cores. q, k, v: [B, H, N, d] bf16 CUDA tensors."""
+def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None, want_lse: bool = True,
+                   skip_underflow: bool = False):
+    """bf16 causal prefill on the tensor cores. q, k, v: [B, H, N, d] bf16 CUDA tensors.
+
+    ``skip_underflow`` leaves out KV tiles whose weights provably flush to zero
+    (alibi_attn_fwd_ex with ALIBI_FWD_SKIP_UNDERFLOW); the result is bit-identical.
+    """
     import torch
     _need(q, torch.bfloat16, None, "q")
     B, H, N, d = q.shape
@@ -148,9 +158,52 @@ def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if lse is not None:
         _need(lse, torch.float32, (B, H, N), "lse")
-    _check(load().alibi_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
-                                 _stream(stream, q.device)), "alibi_attn_fwd")
+    if skip_underflow:
+        _check(load().alibi_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                        int(bool(causal)), ALIBI_FWD_SKIP_UNDERFLOW, 0.0, 0.0,
+                                        _stream(stream, q.device)),
+               "alibi_attn_fwd_ex")
+    else:
+        _check(load().alibi_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                     int(bool(causal)), _stream(stream, q.device)), "alibi_attn_fwd")
     return out, lse
+
+
+def alibi_attn_fwd_ex(q, k, v, out=None, lse=None, causal: bool = True, flags: int = 0, clamp_min: float = -87.0,
+                      softcap_z: float = 50.0, stream=None):
+    """Prefill with options (ALIBI_FWD_* flags): exact underflow skipping, or the
+    clamp / log-distance / soft-cap mitigations with their parameters."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.bfloat16, q.shape, "k")
+    _need(v, torch.bfloat16, q.shape, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, q.shape, "out")
+    _need(lse, torch.float32, (B, H, N), "lse")
+    _check(load().alibi_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                    int(flags), float(clamp_min), float(softcap_z), _stream(stream, q.device)),
+           "alibi_attn_fwd_ex")
+    return out, lse
+
+
+def alibi_attn_skip_plan(q, k, first_tile=None, stream=None):
+    """Per work item (b*H + h, 256-row block): the first 128-key tile the skipping
+    prefill computes. Returns an int32 CUDA tensor [B*H*ceil(N/256)]."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.bfloat16, q.shape, "k")
+    items = B * H * ((N + 255) // 256)
+    if first_tile is None:
+        first_tile = torch.empty(items, dtype=torch.int32, device=q.device)
+    _need(first_tile, torch.int32, (items,), "first_tile")
+    _check(load().alibi_attn_skip_plan(_ptr(q), _ptr(k), B, H, N, d, _ptr(first_tile), _stream(stream, q.device)),
+           "alibi_attn_skip_plan")
+    return first_tile
 
 
 def alibi_attn_fwd_f32(q, k, v, out=None, lse=None, causal: bool = True, stream=None):

@@ -68,6 +68,13 @@ struct FwdParams {
     uint32_t *err;
     int N, BH, H, NQB, NQT, num_items;
     float c1;  // log2(e) / sqrt(d)
+    const int2 *plan;  // optional: work order (item, first KV tile); null = dense, nominal order
+    // Mitigations of "When Attention Goes Blind" sec. 3.4 (kFwdClamp / kFwdLogDist /
+    // kFwdSoftcap bits; 0 = plain ALiBi). Constants in base-2 exponent units:
+    unsigned int variant;
+    float clamp2;  // clamp_min log2(e)
+    float cap_k;   // 2 log2(e) / (sqrt(d) z): 2^(s cap_k) = e^(2 A / z)
+    float cap_zl;  // z log2(e)
     Slopes slopes;
 };
 
@@ -78,9 +85,25 @@ enum : uint32_t {
 };
 
 struct Item {
-    int bh, qb, n;
+    int bh, qb;
+    int top;  // first KV tile visited (the diagonal of the item's upper Q tile)
+    int n;    // KV tiles visited: top, top - 1, ..., top - n + 1
     bool q1valid;
 };
+
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ float max3f(float a, float b, float c)
 {
@@ -109,15 +132,28 @@ __device__ __forceinline__ int item_index(int k)
     return (k & 1) ? (k + 1) * G - 1 - c : k * G + c;
 }
 
-__device__ __forceinline__ Item decode_item(const FwdParams &p, int w)
+// Work item at position idx of the schedule. Without a plan, items are taken
+// longest-first: round r holds the 256-row block NQB-1-r of every (b, h). With a
+// plan (underflow skipping), the plan gives the item and the first KV tile worth
+// computing, already sorted by the tiles the item spans.
+__device__ __forceinline__ Item decode_item(const FwdParams &p, int idx)
 {
     Item it;
-    const int round = w / p.BH;
-    it.bh = w - round * p.BH;
-    it.qb = p.NQB - 1 - round;
+    int first = 0;
+    if (p.plan) {
+        const int2 e = p.plan[idx];
+        it.bh = e.x / p.NQB;
+        it.qb = e.x - it.bh * p.NQB;
+        first = e.y;
+    } else {
+        const int round = idx / p.BH;
+        it.bh = idx - round * p.BH;
+        it.qb = p.NQB - 1 - round;
+    }
     const int qt1 = 2 * it.qb + 1;
     it.q1valid = qt1 < p.NQT;
-    it.n = it.q1valid ? qt1 + 1 : qt1;  // KV tiles 0 .. n-1
+    it.top = it.q1valid ? qt1 : qt1 - 1;
+    it.n = it.top + 1 - first;
     return it;
 }
 
@@ -127,7 +163,9 @@ __device__ __forceinline__ bool slot_active(const Item &t, int s, int it)
     return s == 1 ? t.q1valid : (t.q1valid ? it >= 1 : true);
 }
 
-template <int D>
+// VAR: compiled with the sec. 3.4 mitigation path (p.variant selects which ones);
+// the plain ALiBi kernel (VAR = false) carries none of that code.
+template <int D, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p)
 {
     using C = Cfg<D>;
@@ -214,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 };
                 // order: K(0), K(1), V(0), K(2), V(1), ..., V(n-1)
                 for (int it = 0; it < t.n && ok; ++it) {
-                    ok = load_kv(&p.tk, C::kK, k_full, k_empty, kc, t.n - 1 - it, SITE_PROD_K);
-                    if (ok && it >= 1) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, t.n - it, SITE_PROD_V);
+                    ok = load_kv(&p.tk, C::kK, k_full, k_empty, kc, t.top - it, SITE_PROD_K);
+                    if (ok && it >= 1) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, t.top - (it - 1), SITE_PROD_V);
                 }
-                if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, 0, SITE_PROD_V);
+                if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, t.top - (t.n - 1), SITE_PROD_V);
             }
         }
     } else if (warp == 1) {
@@ -343,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int it0 = (s == 0 && t.q1valid) ? 1 : 0;
             float M = -INFINITY, l = 0.f;
             for (int it = it0; it < t.n; ++it) {
-                const int j = t.n - 1 - it;
+                const int j = t.top - it;
                 ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_SM_S);
                 ++s_cnt;
                 ok = __all_sync(0xffffffffu, ok);  // keep the warp converged for tcgen05.ld
@@ -360,6 +398,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const float nb = -sl2 * static_cast<float>(i - j * BN);
                 const float2 c1v = make_float2(p.c1, p.c1);
                 float x[BN];
+                if (VAR) {
+                    // Mitigation variants, element by element in base-2 units:
+                    //   content  A = s / sqrt(d), soft-capped to z tanh(A / z) with
+                    //            tanh(y) = 1 - 2 / (e^{2y} + 1);
+                    //   distance D = i - (k0 + c), or ln(D + 1); bias -m D (as
+                    //            -m log2(D + 1) in base 2), clamped from below.
+                    const bool cap = p.variant & kFwdSoftcap, logd = p.variant & kFwdLogDist,
+                               clamp = p.variant & kFwdClamp;
+                    const float mnat = p.slopes.nat[t.bh % p.H];
+                    const float dp1 = static_cast<float>(i - j * BN + 1);
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) {
+                        const float sv = __uint_as_float(sraw[c]);
+                        const float a = cap ? fmaf(-2.0f * p.cap_zl, rcp_approx(ex2_approx(sv * p.cap_k) + 1.0f), p.cap_zl)
+                                            : sv * p.c1;
+                        float b = logd ? -mnat * lg2_approx(dp1 - static_cast<float>(c))
+                                       : fmaf(sl2, static_cast<float>(c), nb);
+                        if (clamp) b = fmaxf(b, p.clamp2);
+                        x[c] = a + b;
+                    }
+                } else {
 #pragma unroll
                 for (int u = 0; u < BN / 2; ++u) {
                     const float2 b = make_float2(fmaf(sl2, static_cast<float>(2 * u), nb),
@@ -368,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         __ffma2_rn(make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, b);
                     x[2 * u] = xv.x;
                     x[2 * u + 1] = xv.y;
+                }
                 }
                 if (j == qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
@@ -465,9 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 }  // namespace
 
-template <int D>
+template <int D, bool VAR>
 static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, void *out, float *lse, int B,
-                                   int H, int N, const Slopes &slopes, cudaStream_t stream)
+                                   int H, int N, const Slopes &slopes, const int2 *plan, unsigned int variant,
+                                   float clamp_min, float softcap_z, cudaStream_t stream)
 {
     using C = Cfg<D>;
     FwdParams p;
@@ -487,6 +548,11 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     p.num_items = p.NQB * p.BH;
     p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     p.slopes = slopes;
+    p.plan = plan;
+    p.variant = variant & (kFwdClamp | kFwdLogDist | kFwdSoftcap);
+    p.clamp2 = clamp_min * 1.4426950408889634f;
+    p.cap_k = (variant & kFwdSoftcap) ? 2.0f * 1.4426950408889634f / (sqrtf(static_cast<float>(D)) * softcap_z) : 0.f;
+    p.cap_zl = softcap_z * 1.4426950408889634f;
 
     static bool attr_set = false;  // per process; the attribute is per function
     if (!attr_set) {
@@ -494,24 +560,46 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
         // kLaunchRegs per thread; refuse to launch otherwise (an unbalanced
         // setmaxnreg.inc would wait for registers that never come).
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, VAR>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        e = cudaFuncSetAttribute(fwd_tc_kernel<D, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    fwd_tc_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(p);
+    fwd_tc_kernel<D, VAR><<<grid, kThreads, C::kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
-                          int d, const Slopes &slopes, cudaStream_t stream)
+                          int d, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
+                          cudaStream_t stream)
 {
-    if (d == 128) return launch_fwd_tc_d<128>(q, k, v, out, lse, B, H, N, slopes, stream);
-    if (d == 64) return launch_fwd_tc_d<64>(q, k, v, out, lse, B, H, N, slopes, stream);
-    return cudaErrorInvalidValue;
+    if (d != 128 && d != 64) return cudaErrorInvalidValue;
+    auto run = [&](const int2 *plan) {
+        const bool var = (flags & (kFwdClamp | kFwdLogDist | kFwdSoftcap)) != 0;
+        if (d == 128)
+            return var ? launch_fwd_tc_d<128, true>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min,
+                                                    softcap_z, stream)
+                       : launch_fwd_tc_d<128, false>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min,
+                                                     softcap_z, stream);
+        return var ? launch_fwd_tc_d<64, true>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min, softcap_z,
+                                               stream)
+                   : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min,
+                                                softcap_z, stream);
+    };
+    if (!(flags & kFwdSkipUnderflow)) return run(nullptr);
+    // underflow skipping: the plan lives in a stream-ordered scratch buffer for this call
+    const int NQT = (N + BM - 1) / BM, NQB = (NQT + 1) / 2;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, NQB), decode_pool(), stream);
+    if (e != cudaSuccess) return e;
+    int2 *plan = nullptr;
+    e = launch_skip_plan(q, k, B, H, N, d, slopes, ws, &plan, nullptr, stream);
+    if (e == cudaSuccess) e = run(plan);
+    const cudaError_t f = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace alibi

@@ -196,6 +196,12 @@ static int check_dims(int B, int H, int N, int d)
 int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
                    int causal, void *stream)
 {
+    return alibi_attn_fwd_ex(q, k, v, out, lse, B, H, N, d, causal, 0u, 0.0f, 0.0f, stream);
+}
+
+int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
+                      int d, int causal, unsigned int flags, float clamp_min, float softcap_z, void *stream)
+{
     if (!q || !k || !v || !out) return ALIBI_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && !aligned16(lse)))
         return ALIBI_ERR_INVALID;
@@ -204,9 +210,40 @@ int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float
     if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
     if (causal == 0) return ALIBI_ERR_UNSUPPORTED;
     if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    const unsigned int known = ALIBI_FWD_SKIP_UNDERFLOW | ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP;
+    if (flags & ~known) return ALIBI_ERR_INVALID;
+    if ((flags & ALIBI_FWD_CLAMP) && !(clamp_min < 0.0f)) return ALIBI_ERR_INVALID;
+    if ((flags & ALIBI_FWD_SOFTCAP) && !(softcap_z > 0.0f && std::isfinite(softcap_z))) return ALIBI_ERR_INVALID;
+    if ((flags & ALIBI_FWD_SKIP_UNDERFLOW) && (flags & (ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP)))
+        return ALIBI_ERR_INVALID;
     Slopes s;
     fill_slopes(H, &s);
-    return to_status(launch_fwd_tc(q, k, v, out, lse, B, H, N, d, s, static_cast<cudaStream_t>(stream)));
+    return to_status(launch_fwd_tc(q, k, v, out, lse, B, H, N, d, flags, clamp_min, softcap_z, s,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, int *first_tile, void *stream)
+{
+    if (!q || !k || !first_tile) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(first_tile) & 3u)) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int NQB = ((N + 127) / 128 + 1) / 2, items = B * H * NQB;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, NQB), decode_pool(), cs) != cudaSuccess)
+        return ALIBI_ERR_CUDA;
+    int2 *info = nullptr;
+    cudaError_t e = launch_skip_plan(q, k, B, H, N, d, s, ws, nullptr, &info, cs);
+    // first tiles are the .x fields of the int2 info records
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(first_tile, sizeof(int), info, sizeof(int2), sizeof(int), items,
+                              cudaMemcpyDeviceToDevice, cs);
+    const cudaError_t f = cudaFreeAsync(ws, cs);
+    return to_status(e != cudaSuccess ? e : f);
 }
 
 int alibi_attn_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B, int H, int N,

@@ -41,9 +41,22 @@ size_t decode_partials_bytes(int BH, int splits);
 cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L,
                                const Slopes &slopes, int splits, float *partials, cudaStream_t stream);
 
+// Prefill flags (the values of ALIBI_FWD_* in alibi.h).
+constexpr unsigned int kFwdSkipUnderflow = 1u;
+constexpr unsigned int kFwdClamp = 2u;
+constexpr unsigned int kFwdLogDist = 4u;
+constexpr unsigned int kFwdSoftcap = 8u;
+
+// Underflow-skip plan (alibi_skip.cu): scratch size for B*H heads and NQB 256-row
+// blocks, and the launch that fills it ([plan | info | key norms]).
+size_t skip_plan_bytes(int BH, int NQB);
+cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const Slopes &slopes,
+                             void *scratch, int2 **plan_out, int2 **info_out, cudaStream_t stream);
+
 // Kernel launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
-                          int N, int d, const Slopes &slopes, cudaStream_t stream);
+                          int N, int d, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
+                          cudaStream_t stream);
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B,
                            int H, int N, int d, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N,

@@ -325,6 +325,39 @@ def run_native(args):
             dist.destroy_process_group()
         return
 
+    # -------------------- exact underflow-tile skipping (NEXT-2), same inputs, own timing
+    skip = None
+    if do_pre:
+        plan = ab.alibi_attn_skip_plan(q, k).cpu().numpy()
+        NQB, NQT = (wp.N + 255) // 256, (wp.N + 127) // 128
+        tiles_all = tiles_run = 0
+        for w_i, first in enumerate(plan):
+            qb = w_i % NQB
+            for qt in (2 * qb, 2 * qb + 1):
+                if qt < NQT:
+                    tiles_all += qt + 1
+                    tiles_run += qt + 1 - min(int(first), qt + 1)
+        for _ in range(args.warmup):
+            ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for s_i in range(args.steps):
+            flush.fill_(1.0)
+            ev[s_i][0].record(stream)
+            ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True)
+            ev[s_i][1].record(stream)
+        torch.cuda.synchronize()
+        t_skip = torch.tensor([sum(e[0].elapsed_time(e[1]) for e in ev)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t_skip, op=dist.ReduceOp.MAX)
+        t_skip = float(t_skip[0]) / args.steps
+        tile_flops = 4.0 * 128 * 128 * wp.d  # QK^T + PV of one 128 x 128 tile
+        skip = {"ms": t_skip, "launches": 4,  # key norms, item plan, plan sort, prefill
+                "algorithmic_tflops": world * prefill_flops(wp) / (t_skip / 1e3) / 1e12,
+                "executed_tflops": world * tiles_run * tile_flops / (t_skip / 1e3) / 1e12,
+                "tiles_skipped_frac": 1.0 - tiles_run / tiles_all,
+                "exact": "bit-identical to the dense kernel (tested)"}
+        ab.alibi_check_error(stream)
+
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
     e2e_dec = None
@@ -440,6 +473,7 @@ def run_native(args):
             "e2e": e2e_dec,
         },
         "underflow": underflow,
+        "prefill_skip_underflow": skip,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,

@@ -80,6 +80,46 @@ ALIBI_API int alibi_slopes(int H, float *out_host);
 ALIBI_API int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
                    int B, int H, int N, int d, int causal, void *stream);
 
+/* Flags of alibi_attn_fwd_ex. */
+#define ALIBI_FWD_SKIP_UNDERFLOW 1u /* leave out tiles whose weights flush to zero (exact)   */
+#define ALIBI_FWD_CLAMP 2u          /* bias B* = max(B, clamp_min)                          */
+#define ALIBI_FWD_LOGDIST 4u        /* distance D* = ln(D + 1)                              */
+#define ALIBI_FWD_SOFTCAP 8u        /* content score A* = z tanh(A / z), z = softcap_z      */
+
+/*
+ * alibi_attn_fwd with options; flags = 0 is exactly alibi_attn_fwd.
+ *
+ * ALIBI_FWD_SKIP_UNDERFLOW: leave out the KV tiles at the far end of each
+ * query block's causal range whose weights provably flush to zero ("When
+ * Attention Goes Blind", sec. 3.2-3.3: past the blindness distance the
+ * exponent falls below the smallest normal number; sec. 5.2: steep heads act
+ * as a sliding window). A pre-pass bounds every score by |q_i| max_j |k_j| and
+ * the running max from below by the diagonal score; a tile is left out only if
+ * every exponent in it is below -127 (base 2), where the kernel's
+ * flush-to-zero exponential returns exactly 0. Output and LSE are therefore
+ * bit-identical to flags = 0. The pre-pass reads Q and K once and takes a
+ * small plan buffer (items x 16 bytes) from the library's stream-ordered pool.
+ *
+ * ALIBI_FWD_CLAMP / _LOGDIST / _SOFTCAP: the mitigations of "When Attention
+ * Goes Blind", sec. 3.4 (the paper trains with clamp_min = -87, sec. 4.3, and
+ * z = 50). clamp_min is in natural-log units and must be < 0; softcap_z > 0.
+ * They cannot be combined with ALIBI_FWD_SKIP_UNDERFLOW (clamped or
+ * log-scaled biases do not underflow). Unused float arguments are ignored.
+ */
+ALIBI_API int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse,
+                   int B, int H, int N, int d, int causal, unsigned int flags, float clamp_min,
+                   float softcap_z, void *stream);
+
+/*
+ * The skip plan alone (analysis and tests): for each work item w = (b*H + h) *
+ * ceil(N/256) + blk (query rows [256 blk, 256 blk + 256) of head (b, h)),
+ * first_tile[w] is the first 128-key tile the skipping kernel computes; tiles
+ * 0 .. first_tile[w]-1 are left out. first_tile: device int32 [B*H*ceil(N/256)].
+ * d in {64, 128}.
+ */
+ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, int *first_tile,
+                   void *stream);
+
 /*
  * Causal prefill in fp32 (reference precision): all inputs, outputs and
  * arithmetic in fp32 on the CUDA cores with IEEE expf. Same layouts and

@@ -106,6 +106,18 @@ def test_fwd_argument_errors(lib):
     assert f(P, P, P, P, P, 1, 300, 8, 64, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
 
 
+def test_fwd_ex_flags_and_plan_errors(lib):
+    f = lib.alibi_attn_fwd_ex
+    U, F = ctypes.c_uint, ctypes.c_float
+    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(16), F(0), F(0), None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, 1, 1, 8, 32, 1, U(1), F(0), F(0), None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(2), F(1.0), F(0), None) == ab.ALIBI_ERR_INVALID   # clamp >= 0
+    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(8), F(0), F(-5.0), None) == ab.ALIBI_ERR_INVALID  # z <= 0
+    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(1 | 4), F(0), F(0), None) == ab.ALIBI_ERR_INVALID  # skip + logdist
+    assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 64, None, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 48, P, None) == ab.ALIBI_ERR_UNSUPPORTED
+
+
 def test_decode_and_aux_argument_errors(lib):
     assert lib.alibi_attn_decode(None, P, P, P, 1, 1, 8, 128, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 0, 128, None) == ab.ALIBI_ERR_INVALID
