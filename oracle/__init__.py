@@ -60,6 +60,7 @@ def _load():
         lib.oracle_slope_exponent.argtypes = [I, I, P(I), P(I)]
         lib.oracle_slopes.argtypes = [I, f64p]
         lib.oracle_slopes_f32.argtypes = [I, f32p]
+        lib.oracle_slopes_explicit.argtypes = [I, D, D, D, I, f64p]
         lib.oracle_bias.argtypes = [D, ctypes.c_long, ctypes.c_long, I]
         lib.oracle_bias.restype = D
         lib.oracle_bias_ex.argtypes = [D, ctypes.c_long, ctypes.c_long, I, I, D]
@@ -110,6 +111,18 @@ def slopes_f32(H: int) -> np.ndarray:
     """ALiBi slopes rounded once to fp32."""
     m = np.empty(H, dtype=np.float32)
     _check(_load().oracle_slopes_f32(H, _ptr(m, ctypes.c_float)))
+    return m
+
+
+def slopes_explicit(H: int, delta_first: float, delta_last: float, tau: float | None = None,
+                    log_distance: bool = False) -> np.ndarray:
+    """fp64 slopes whose zero-logit blindness distances run geometrically from
+    delta_first to delta_last ("When Attention Goes Blind", sec. 3.4 "Robust
+    Slopes", sec. 4.3, Table 8). tau defaults to ln 2^-126."""
+    tau = tau_denorm() if tau is None else float(tau)
+    m = np.empty(H, dtype=np.float64)
+    _check(_load().oracle_slopes_explicit(int(H), float(delta_first), float(delta_last), tau,
+                                          int(bool(log_distance)), _ptr(m, ctypes.c_double)))
     return m
 
 

@@ -108,6 +108,30 @@ int oracle_slopes_f32(int H, float *m)
     return ORACLE_OK;
 }
 
+/*
+ * Slopes chosen from target blindness distances ("When Attention Goes Blind",
+ * sec. 3.4 "Robust Slopes"; sec. 4.2 "Positional Encoding Configurations";
+ * sec. 4.3 for the log-distance adaptation; App. F Table 8 for the schedules).
+ * The targets run geometrically from delta_first (head 0) to delta_last
+ * (head H - 1):
+ *   delta_h = delta_first * (delta_last / delta_first)^(h / (H - 1)),
+ * and each slope puts the zero-logit crossing exactly at its target, i.e.
+ * solves -m delta_h = tau (linear distances) or -m log(delta_h + 1) = tau
+ * (log-scaled distances, the E+L combination). H = 1 takes delta_first.
+ */
+int oracle_slopes_explicit(int H, double delta_first, double delta_last, double tau, int log_distance, double *m)
+{
+    if (H < 1 || !m || !(delta_first > 0.0) || !(delta_last > 0.0) || !(tau < 0.0)) return ORACLE_EINVAL;
+    if (!isfinite(delta_first) || !isfinite(delta_last) || !isfinite(tau)) return ORACLE_EINVAL;
+    for (int h = 0; h < H; ++h) {
+        double t = H > 1 ? (double)h / (double)(H - 1) : 0.0;
+        double delta = delta_first * pow(delta_last / delta_first, t);
+        double dist = log_distance ? log(delta + 1.0) : delta;
+        m[h] = -tau / dist;
+    }
+    return ORACLE_OK;
+}
+
 /* -------------------------------------------------------------------- bias */
 
 /*

@@ -395,3 +395,59 @@ def test_softcap_variant():
     assert lse[0, 0, 0] == pytest.approx(50.0 * math.tanh(2.0), abs=1e-12)
     _, lse_plain, _ = oracle.attention(q, q, q, m=np.array([0.5]))
     assert lse_plain[0, 0, 0] == pytest.approx(100.0, abs=1e-12)
+
+
+# Table 8 ("When Attention Goes Blind", App. F): expected blindness distances of
+# the trained 9-head models, rounded to the nearest integer.
+TABLE8_SCHEDULES = {
+    "Steep": (128, 512, [128, 152, 181, 215, 256, 304, 362, 431, 512]),
+    "Safe": (2048, 4096, [2048, 2233, 2435, 2656, 2896, 3158, 3444, 3756, 4096]),
+    "Wide": (16, 4096, [16, 32, 64, 128, 256, 512, 1024, 2048, 4096]),
+    "Explicit": (32, 8192, [32, 64, 128, 256, 512, 1024, 2048, 4096, 8192]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TABLE8_SCHEDULES))
+def test_table8_explicit_schedules(name):
+    # sec. 4.2 names only delta_1 and delta_H for Steep / Safe / Wide; Table 8's
+    # middle columns fix the spacing as geometric over the nine heads.
+    d1, dH, want = TABLE8_SCHEDULES[name]
+    m = oracle.slopes_explicit(9, d1, dH)
+    assert [round(oracle.blindness_real(x)) for x in m] == want
+    # slopes fall head by head and the steepest head is the first
+    assert np.all(np.diff(m) < 0)
+
+
+def test_explicit_slopes_section_3_4_example():
+    # sec. 3.4 "Robust Slopes": for a 2048 context the targets double from 32
+    # to 2048, i.e. seven heads.
+    m = oracle.slopes_explicit(7, 32, 2048)
+    assert [round(oracle.blindness_real(x)) for x in m] == [32, 64, 128, 256, 512, 1024, 2048]
+    # the crossing sits on the target up to rounding, so the integer definition
+    # lands on it or one token past it
+    for x, want in zip(m, [32, 64, 128, 256, 512, 1024, 2048]):
+        assert oracle.blindness_int(x) in (want, want + 1)
+
+
+def test_explicit_slopes_log_distance_adaptation():
+    # sec. 4.3: with log-scaled distances (E+L) the slopes become
+    # m_h = -tau / log(delta_h + 1), so the log-distance crossing lands on delta_h.
+    m = oracle.slopes_explicit(9, 32, 8192, log_distance=True)
+    for x, want in zip(m, TABLE8_SCHEDULES["Explicit"][2]):
+        assert math.isclose(oracle.blindness_real(x, log_distance=True), want, rel_tol=1e-9)
+        assert math.isclose(x, -TAU_D / math.log(want + 1), rel_tol=1e-12)
+    # with linear distances the same slopes go blind after only log(delta + 1) tokens
+    assert round(oracle.blindness_real(m[0])) == round(math.log(33))
+
+
+def test_explicit_slopes_edges():
+    # one head takes delta_first; equal ends give equal slopes; tau scales them
+    assert math.isclose(oracle.slopes_explicit(1, 100, 5000)[0], -TAU_D / 100, rel_tol=1e-15)
+    assert np.allclose(oracle.slopes_explicit(4, 300, 300), -TAU_D / 300, rtol=1e-15)
+    assert np.allclose(oracle.slopes_explicit(5, 16, 256, tau=-1.0), 1.0 / (16 * 2.0 ** np.arange(5)),
+                       rtol=1e-14)
+    for bad in [(0, 16, 64), (4, 0, 64), (4, 16, -1), (4, 16, float("inf"))]:
+        with pytest.raises(RuntimeError):
+            oracle.slopes_explicit(*bad)
+    with pytest.raises(RuntimeError):
+        oracle.slopes_explicit(4, 16, 64, tau=0.5)
