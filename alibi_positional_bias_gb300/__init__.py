@@ -1,4 +1,4 @@
-"""GB300-native ALiBi causal attention: Python binding of the C ABI (include/alibi.h).
+"""GB300-native ALiBi attention: Python binding of the C ABI (include/alibi.h).
 
 Argument marshalling only: every step of the computation runs in the CUDA
 library ``_build/libalibi_gb300.so``. There is no CPU fallback; if the library
@@ -11,6 +11,7 @@ torch's current stream on the tensors' device.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 
@@ -22,6 +23,7 @@ __all__ = [
     "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
     "alibi_attn_fwd", "alibi_attn_fwd_ex", "alibi_attn_skip_plan", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
     "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc", "alibi_selftest_timeout",
+    "alibi_slopes_explicit", "alibi_attn_probs_f32_ex", "AlibiFwdOptions",
 ]
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
@@ -29,6 +31,12 @@ ALIBI_FWD_SKIP_UNDERFLOW, ALIBI_FWD_CLAMP, ALIBI_FWD_LOGDIST, ALIBI_FWD_SOFTCAP 
 
 _lock = threading.Lock()
 _lib = None
+
+
+class AlibiFwdOptions(ctypes.Structure):
+    """The C struct alibi_fwd_options (include/alibi.h)."""
+    _fields_ = [("flags", ctypes.c_uint), ("clamp_min", ctypes.c_float), ("softcap_z", ctypes.c_float),
+                ("slopes", ctypes.POINTER(ctypes.c_float))]
 
 
 class AlibiError(RuntimeError):
@@ -60,7 +68,10 @@ def load(build_if_missing: bool = False):
         lib.alibi_slopes.argtypes = [I, ctypes.POINTER(F)]
         lib.alibi_attn_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
-        lib.alibi_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, ctypes.c_uint, F, F, vp]
+        lib.alibi_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, ctypes.POINTER(AlibiFwdOptions), vp]
+        lib.alibi_slopes_explicit.argtypes = [I, ctypes.c_double, ctypes.c_double, ctypes.c_double, I,
+                                              ctypes.POINTER(F)]
+        lib.alibi_attn_probs_f32_ex.argtypes = [vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_fwd_ex.restype = I
         lib.alibi_attn_skip_plan.argtypes = [vp, vp, I, I, I, I, vp, vp]
         lib.alibi_attn_skip_plan.restype = I
@@ -141,7 +152,8 @@ def alibi_slopes(H: int) -> np.ndarray:
 
 def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None, want_lse: bool = True,
                    skip_underflow: bool = False):
-    """bf16 causal prefill on the tensor cores. q, k, v: [B, H, N, d] bf16 CUDA tensors.
+    """bf16 prefill on the tensor cores (causal, or symmetric bias over all keys).
+    q, k, v: [B, H, N, d] bf16 CUDA tensors.
 
     ``skip_underflow`` leaves out KV tiles whose weights provably flush to zero
     (alibi_attn_fwd_ex with ALIBI_FWD_SKIP_UNDERFLOW); the result is bit-identical.
@@ -159,9 +171,9 @@ def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None
     if lse is not None:
         _need(lse, torch.float32, (B, H, N), "lse")
     if skip_underflow:
+        opt = AlibiFwdOptions(ALIBI_FWD_SKIP_UNDERFLOW, 0.0, 0.0, None)
         _check(load().alibi_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
-                                        int(bool(causal)), ALIBI_FWD_SKIP_UNDERFLOW, 0.0, 0.0,
-                                        _stream(stream, q.device)),
+                                        int(bool(causal)), ctypes.byref(opt), _stream(stream, q.device)),
                "alibi_attn_fwd_ex")
     else:
         _check(load().alibi_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
@@ -170,9 +182,10 @@ def alibi_attn_fwd(q, k, v, out=None, lse=None, causal: bool = True, stream=None
 
 
 def alibi_attn_fwd_ex(q, k, v, out=None, lse=None, causal: bool = True, flags: int = 0, clamp_min: float = -87.0,
-                      softcap_z: float = 50.0, stream=None):
+                      softcap_z: float = 50.0, slopes=None, stream=None):
     """Prefill with options (ALIBI_FWD_* flags): exact underflow skipping, or the
-    clamp / log-distance / soft-cap mitigations with their parameters."""
+    clamp / log-distance / soft-cap mitigations with their parameters, and
+    optionally caller-chosen per-head slopes (H values, natural-log units)."""
     import torch
     _need(q, torch.bfloat16, None, "q")
     B, H, N, d = q.shape
@@ -184,10 +197,29 @@ def alibi_attn_fwd_ex(q, k, v, out=None, lse=None, causal: bool = True, flags: i
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _need(out, torch.bfloat16, q.shape, "out")
     _need(lse, torch.float32, (B, H, N), "lse")
+    m = None
+    if slopes is not None:
+        m = np.ascontiguousarray(slopes, dtype=np.float32)
+        if m.shape != (H,):
+            raise ValueError(f"slopes: expected shape ({H},), got {m.shape}")
+    opt = AlibiFwdOptions(int(flags), float(clamp_min), float(softcap_z),
+                          None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     _check(load().alibi_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
-                                    int(flags), float(clamp_min), float(softcap_z), _stream(stream, q.device)),
+                                    ctypes.byref(opt), _stream(stream, q.device)),
            "alibi_attn_fwd_ex")
     return out, lse
+
+
+def alibi_slopes_explicit(H: int, delta_first: float, delta_last: float, tau: float | None = None,
+                          log_distance: bool = False) -> np.ndarray:
+    """fp32 slopes whose zero-logit blindness distances run geometrically from
+    delta_first (head 0) to delta_last (head H-1); tau defaults to ln 2^-126."""
+    tau = -126.0 * math.log(2.0) if tau is None else tau
+    out = np.empty(H, dtype=np.float32)
+    _check(load().alibi_slopes_explicit(int(H), float(delta_first), float(delta_last), float(tau),
+                                        int(bool(log_distance)), out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))),
+           "alibi_slopes_explicit")
+    return out
 
 
 def alibi_attn_skip_plan(q, k, first_tile=None, stream=None):
@@ -207,7 +239,7 @@ def alibi_attn_skip_plan(q, k, first_tile=None, stream=None):
 
 
 def alibi_attn_fwd_f32(q, k, v, out=None, lse=None, causal: bool = True, stream=None):
-    """fp32 causal prefill (reference precision). q, k, v: [B, H, N, d] fp32 CUDA tensors."""
+    """fp32 prefill (reference precision), causal or symmetric. q, k, v: [B, H, N, d] fp32 CUDA tensors."""
     import torch
     _need(q, torch.float32, None, "q")
     B, H, N, d = q.shape
@@ -266,7 +298,12 @@ def alibi_attn_decode_splits(B: int, H: int, L: int, d: int) -> int:
 
 
 def alibi_attn_probs_f32(q, k, lse, P=None, stream=None):
-    """fp32 attention weights [B, H, N, N] from the LSE of alibi_attn_fwd_f32."""
+    """fp32 causal attention weights [B, H, N, N] from the LSE of alibi_attn_fwd_f32."""
+    return alibi_attn_probs_f32_ex(q, k, lse, P, causal=True, stream=stream)
+
+
+def alibi_attn_probs_f32_ex(q, k, lse, P=None, causal: bool = True, stream=None):
+    """fp32 attention weights [B, H, N, N] from the LSE of alibi_attn_fwd_f32 (either mask)."""
     import torch
     _need(q, torch.float32, None, "q")
     B, H, N, d = q.shape
@@ -275,8 +312,8 @@ def alibi_attn_probs_f32(q, k, lse, P=None, stream=None):
     if P is None:
         P = torch.empty((B, H, N, N), dtype=torch.float32, device=q.device)
     _need(P, torch.float32, (B, H, N, N), "P")
-    _check(load().alibi_attn_probs_f32(_ptr(q), _ptr(k), _ptr(lse), _ptr(P), B, H, N, d,
-                                       _stream(stream, q.device)), "alibi_attn_probs_f32")
+    _check(load().alibi_attn_probs_f32_ex(_ptr(q), _ptr(k), _ptr(lse), _ptr(P), B, H, N, d, int(bool(causal)),
+                                          _stream(stream, q.device)), "alibi_attn_probs_f32_ex")
     return P
 
 

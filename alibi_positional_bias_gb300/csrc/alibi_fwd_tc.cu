@@ -1,7 +1,9 @@
-// Causal ALiBi prefill on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+// ALiBi prefill on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // Computes, per (b, h) and query row i,
-//   x_ij = q_i.k_j / sqrt(d) - m_h (i - j)   for j <= i        (keys j > i masked)
+//   x_ij = q_i.k_j / sqrt(d) - m_h (i - j)   for j <= i        (causal: keys j > i masked)
+//   x_ij = q_i.k_j / sqrt(d) - m_h |i - j|   for all j < N     (non-causal, symmetric bias
+//          of "ALiBi and Relative Position Bias" (quantmemo.com), "The mechanics")
 //   O_i  = sum_j softmax_j(x_ij) v_j,   LSE_i = ln sum_j exp(x_ij)
 // following "When Attention Goes Blind: Numerical Failure in ALiBi Positional
 // Encodings" (arXiv 2608.03994) sec. 3.1 eq. 1-3 and App. B.1 (max-shifted
@@ -21,8 +23,11 @@
 //               is generated from the integer tile coordinates; the running
 //               max is raised lazily (only when a tile exceeds it by 2^8).
 // A work item is (b*H + h, block of 256 query rows = two 128-row tiles);
-// KV tiles are visited from the diagonal downwards and tiles entirely above
-// the diagonal are never loaded. Items are dealt longest-first in snake order.
+// KV tiles are visited from the diagonal downwards. Causal: tiles entirely
+// above the diagonal are never loaded. Non-causal: after tile 0 the walk wraps
+// to the last tile and comes back down to the diagonal, so every row meets its
+// largest biases (the diagonal) first. Items are dealt longest-first in snake
+// order.
 //
 // TMEM columns: S/P slot s at [128 s, 128 s + 128), O slot s at 256 + 128 s.
 // P (bf16, two per 32-bit column) overwrites the first 64 columns of S.
@@ -67,6 +72,7 @@ struct FwdParams {
     float *lse;
     uint32_t *err;
     int N, BH, H, NQB, NQT, num_items;
+    int causal;  // 1: keys j <= i only; 0: every key, distance |i - j|
     float c1;  // log2(e) / sqrt(d)
     const int2 *plan;  // optional: work order (item, first KV tile); null = dense, nominal order
     // Mitigations of "When Attention Goes Blind" sec. 3.4 (kFwdClamp / kFwdLogDist /
@@ -87,7 +93,7 @@ enum : uint32_t {
 struct Item {
     int bh, qb;
     int top;  // first KV tile visited (the diagonal of the item's upper Q tile)
-    int n;    // KV tiles visited: top, top - 1, ..., top - n + 1
+    int n;    // KV tiles visited: top, top - 1, ..., then (non-causal) NQT - 1, ..., top + 1
     bool q1valid;
 };
 
@@ -153,14 +159,22 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int idx)
     const int qt1 = 2 * it.qb + 1;
     it.q1valid = qt1 < p.NQT;
     it.top = it.q1valid ? qt1 : qt1 - 1;
-    it.n = it.top + 1 - first;
+    it.n = p.causal ? it.top + 1 - first : p.NQT;
     return it;
 }
 
-// Is Q slot s active at iteration `it` (KV tile n-1-it)?
-__device__ __forceinline__ bool slot_active(const Item &t, int s, int it)
+// KV tile visited at iteration `it` of an item (0 <= it < n).
+__device__ __forceinline__ int kv_tile(const FwdParams &p, const Item &t, int it)
 {
-    return s == 1 ? t.q1valid : (t.q1valid ? it >= 1 : true);
+    const int j = t.top - it;
+    return j >= 0 ? j : j + p.NQT;
+}
+
+// Is Q slot s active at iteration `it`? Causal: slot 0 skips the first tile (the
+// diagonal of slot 1 lies entirely above slot 0's rows). Non-causal: always.
+__device__ __forceinline__ bool slot_active(const FwdParams &p, const Item &t, int s, int it)
+{
+    return s == 1 ? t.q1valid : (t.q1valid && p.causal ? it >= 1 : true);
 }
 
 // VAR: compiled with the sec. 3.4 mitigation path (p.variant selects which ones);
@@ -252,10 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 };
                 // order: K(0), K(1), V(0), K(2), V(1), ..., V(n-1)
                 for (int it = 0; it < t.n && ok; ++it) {
-                    ok = load_kv(&p.tk, C::kK, k_full, k_empty, kc, t.top - it, SITE_PROD_K);
-                    if (ok && it >= 1) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, t.top - (it - 1), SITE_PROD_V);
+                    ok = load_kv(&p.tk, C::kK, k_full, k_empty, kc, kv_tile(p, t, it), SITE_PROD_K);
+                    if (ok && it >= 1)
+                        ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, kv_tile(p, t, it - 1), SITE_PROD_V);
                 }
-                if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, t.top - (t.n - 1), SITE_PROD_V);
+                if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, kv_tile(p, t, t.n - 1), SITE_PROD_V);
             }
         }
     } else if (warp == 1) {
@@ -312,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     ok = mbar_wait(&k_full[st], ph, err, SITE_MMA_K);
                     if (!ok) break;
                     for (int s = 0; s < 2; ++s)
-                        if (slot_active(t, s, 0)) issue_S(s, st);
+                        if (slot_active(p, t, s, 0)) issue_S(s, st);
                     mma_commit(&k_empty[st]);
                 }
                 for (int it = 0; it < t.n && ok; ++it) {
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!ok) break;
                     }
                     for (int s = 0; s < 2 && ok; ++s) {
-                        if (slot_active(t, s, it)) {
+                        if (slot_active(p, t, s, it)) {
                             ok = mbar_wait(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
                             if (ok && first_pv[s]) ok = mbar_wait(&o_empty[s], (o_cnt[s] & 1) ^ 1, err, SITE_MMA_O);
                             if (!ok) break;
@@ -344,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 ++o_cnt[s];
                             }
                         }
-                        if (it + 1 < t.n && slot_active(t, s, it + 1)) {
+                        if (it + 1 < t.n && slot_active(p, t, s, it + 1)) {
                             const uint32_t kst = (kc + it + 1) % 2;
                             issue_S(s, kst);
                             if (s == last_slot) mma_commit(&k_empty[kst]);
@@ -378,10 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int qt = 2 * t.qb + s;
             const int i = qt * BM + r;
             const float sl2 = p.slopes.log2e[t.bh % p.H];
-            const int it0 = (s == 0 && t.q1valid) ? 1 : 0;
+            const int it0 = (s == 0 && t.q1valid && p.causal) ? 1 : 0;
             float M = -INFINITY, l = 0.f;
             for (int it = it0; it < t.n; ++it) {
-                const int j = t.top - it;
+                const int j = kv_tile(p, t, it);
                 ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_SM_S);
                 ++s_cnt;
                 ok = __all_sync(0xffffffffu, ok);  // keep the warp converged for tcgen05.ld
@@ -397,41 +412,69 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // absolute position enters the fp32 arithmetic.
                 const float nb = -sl2 * static_cast<float>(i - j * BN);
                 const float2 c1v = make_float2(p.c1, p.c1);
+                // Non-causal tiles at or right of the diagonal hold keys past the query:
+                // there the distance is |i - k| and the bias -|nb + sl2 c| (sl2 >= 0).
+                const bool sym = !p.causal && j >= qt;
                 float x[BN];
                 if (VAR) {
                     // Mitigation variants, element by element in base-2 units:
                     //   content  A = s / sqrt(d), soft-capped to z tanh(A / z) with
                     //            tanh(y) = 1 - 2 / (e^{2y} + 1);
-                    //   distance D = i - (k0 + c), or ln(D + 1); bias -m D (as
+                    //   distance D = |i - (k0 + c)|, or ln(D + 1); bias -m D (as
                     //            -m log2(D + 1) in base 2), clamped from below.
                     const bool cap = p.variant & kFwdSoftcap, logd = p.variant & kFwdLogDist,
                                clamp = p.variant & kFwdClamp;
                     const float mnat = p.slopes.nat[t.bh % p.H];
-                    const float dp1 = static_cast<float>(i - j * BN + 1);
+                    const float di = static_cast<float>(i - j * BN);  // exact: |i - k0| < 2^24
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
                         const float sv = __uint_as_float(sraw[c]);
                         const float a = cap ? fmaf(-2.0f * p.cap_zl, rcp_approx(ex2_approx(sv * p.cap_k) + 1.0f), p.cap_zl)
                                             : sv * p.c1;
-                        float b = logd ? -mnat * lg2_approx(dp1 - static_cast<float>(c))
-                                       : fmaf(sl2, static_cast<float>(c), nb);
+                        float b;
+                        if (logd) {
+                            b = -mnat * lg2_approx(fabsf(di - static_cast<float>(c)) + 1.0f);
+                        } else {
+                            b = fmaf(sl2, static_cast<float>(c), nb);
+                            if (sym) b = -fabsf(b);
+                        }
                         if (clamp) b = fmaxf(b, p.clamp2);
                         x[c] = a + b;
                     }
+                } else if (!sym) {
+#pragma unroll
+                    for (int u = 0; u < BN / 2; ++u) {
+                        const float2 b = make_float2(fmaf(sl2, static_cast<float>(2 * u), nb),
+                                                     fmaf(sl2, static_cast<float>(2 * u + 1), nb));
+                        const float2 xv = __ffma2_rn(
+                            make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, b);
+                        x[2 * u] = xv.x;
+                        x[2 * u + 1] = xv.y;
+                    }
                 } else {
 #pragma unroll
-                for (int u = 0; u < BN / 2; ++u) {
-                    const float2 b = make_float2(fmaf(sl2, static_cast<float>(2 * u), nb),
-                                                 fmaf(sl2, static_cast<float>(2 * u + 1), nb));
-                    const float2 xv =
-                        __ffma2_rn(make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, b);
-                    x[2 * u] = xv.x;
-                    x[2 * u + 1] = xv.y;
+                    for (int u = 0; u < BN / 2; ++u) {
+                        const float2 b = make_float2(-fabsf(fmaf(sl2, static_cast<float>(2 * u), nb)),
+                                                     -fabsf(fmaf(sl2, static_cast<float>(2 * u + 1), nb)));
+                        const float2 xv = __ffma2_rn(
+                            make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, b);
+                        x[2 * u] = xv.x;
+                        x[2 * u + 1] = xv.y;
+                    }
                 }
-                }
-                if (j == qt) {  // diagonal tile: keys after the query are masked
+                if (p.causal) {
+                    if (j == qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) x[c] = (c > r) ? -INFINITY : x[c];
+                        for (int c = 0; c < BN; ++c) x[c] = (c > r) ? -INFINITY : x[c];
+                    }
+                } else if (j == p.NQT - 1) {
+                    // last tile: the keys past N (zero-filled by TMA) are masked; every
+                    // tile keeps at least its first key, so the row max stays finite
+                    const int kv = p.N - j * BN;
+                    if (kv < BN) {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c) x[c] = (c >= kv) ? -INFINITY : x[c];
+                    }
                 }
                 const float mt = row_max128(x);
                 // Raise the running max lazily: only when this tile exceeds it by 2^8. The
@@ -527,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 template <int D, bool VAR>
 static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, void *out, float *lse, int B,
-                                   int H, int N, const Slopes &slopes, const int2 *plan, unsigned int variant,
+                                   int H, int N, int causal, const Slopes &slopes, const int2 *plan, unsigned int variant,
                                    float clamp_min, float softcap_z, cudaStream_t stream)
 {
     using C = Cfg<D>;
@@ -546,6 +589,7 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     p.NQT = (N + BM - 1) / BM;
     p.NQB = (p.NQT + 1) / 2;
     p.num_items = p.NQB * p.BH;
+    p.causal = causal;
     p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     p.slopes = slopes;
     p.plan = plan;
@@ -573,20 +617,20 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
 }
 
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
-                          int d, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
+                          int d, int causal, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
                           cudaStream_t stream)
 {
     if (d != 128 && d != 64) return cudaErrorInvalidValue;
     auto run = [&](const int2 *plan) {
         const bool var = (flags & (kFwdClamp | kFwdLogDist | kFwdSoftcap)) != 0;
         if (d == 128)
-            return var ? launch_fwd_tc_d<128, true>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min,
+            return var ? launch_fwd_tc_d<128, true>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min,
                                                     softcap_z, stream)
-                       : launch_fwd_tc_d<128, false>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min,
+                       : launch_fwd_tc_d<128, false>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min,
                                                      softcap_z, stream);
-        return var ? launch_fwd_tc_d<64, true>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min, softcap_z,
+        return var ? launch_fwd_tc_d<64, true>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min, softcap_z,
                                                stream)
-                   : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, slopes, plan, flags, clamp_min,
+                   : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min,
                                                 softcap_z, stream);
     };
     if (!(flags & kFwdSkipUnderflow)) return run(nullptr);

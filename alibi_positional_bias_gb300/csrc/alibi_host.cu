@@ -139,6 +139,14 @@ void fill_slopes(int H, Slopes *s)
     }
 }
 
+void fill_slopes_from(int H, const float *nat, Slopes *s)
+{
+    for (int h = 0; h < H && h < kMaxHeads; ++h) {
+        s->nat[h] = nat[h];
+        s->log2e[h] = static_cast<float>(static_cast<double>(nat[h]) * 1.4426950408889634);
+    }
+}
+
 bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                          uint32_t box0, uint32_t box1)
 {
@@ -184,6 +192,23 @@ int alibi_slopes(int H, float *out_host)
     return ALIBI_OK;
 }
 
+int alibi_slopes_explicit(int H, double delta_first, double delta_last, double tau, int log_distance,
+                          float *out_host)
+{
+    if (!out_host || H < 1 || H > 4096 || (log_distance != 0 && log_distance != 1)) return ALIBI_ERR_INVALID;
+    if (!(delta_first > 0.0) || !(delta_last > 0.0) || !(tau < 0.0)) return ALIBI_ERR_INVALID;
+    if (!std::isfinite(delta_first) || !std::isfinite(delta_last) || !std::isfinite(tau)) return ALIBI_ERR_INVALID;
+    // geometric targets in log space: ln delta_h = ln delta_first + (h / (H - 1)) ln(delta_last / delta_first)
+    const double l0 = std::log(delta_first), span = std::log(delta_last) - l0;
+    for (int h = 0; h < H; ++h) {
+        const double delta = H > 1 ? std::exp(l0 + span * h / (H - 1)) : delta_first;
+        // slope whose zero-logit bias reaches tau exactly at the target distance
+        const double dist = log_distance ? std::log1p(delta) : delta;
+        out_host[h] = static_cast<float>(-tau / dist);
+    }
+    return ALIBI_OK;
+}
+
 static int check_dims(int B, int H, int N, int d)
 {
     if (B < 1 || H < 1 || N < 1 || d < 1) return ALIBI_ERR_INVALID;
@@ -196,19 +221,31 @@ static int check_dims(int B, int H, int N, int d)
 int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
                    int causal, void *stream)
 {
-    return alibi_attn_fwd_ex(q, k, v, out, lse, B, H, N, d, causal, 0u, 0.0f, 0.0f, stream);
+    return alibi_attn_fwd_ex(q, k, v, out, lse, B, H, N, d, causal, nullptr, stream);
+}
+
+// Caller-chosen slopes must be finite and non-negative (a zero slope is plain
+// attention; a negative one would reward distance).
+static bool slopes_ok(int H, const float *m)
+{
+    for (int h = 0; h < H; ++h)
+        if (!std::isfinite(m[h]) || m[h] < 0.0f) return false;
+    return true;
 }
 
 int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
-                      int d, int causal, unsigned int flags, float clamp_min, float softcap_z, void *stream)
+                      int d, int causal, const alibi_fwd_options *opt, void *stream)
 {
+    const alibi_fwd_options none = {0u, 0.0f, 0.0f, nullptr};
+    if (!opt) opt = &none;
+    const unsigned int flags = opt->flags;
+    const float clamp_min = opt->clamp_min, softcap_z = opt->softcap_z;
     if (!q || !k || !v || !out) return ALIBI_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && !aligned16(lse)))
         return ALIBI_ERR_INVALID;
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
     if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
-    if (causal == 0) return ALIBI_ERR_UNSUPPORTED;
     if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
     const unsigned int known = ALIBI_FWD_SKIP_UNDERFLOW | ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP;
     if (flags & ~known) return ALIBI_ERR_INVALID;
@@ -216,9 +253,15 @@ int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, fl
     if ((flags & ALIBI_FWD_SOFTCAP) && !(softcap_z > 0.0f && std::isfinite(softcap_z))) return ALIBI_ERR_INVALID;
     if ((flags & ALIBI_FWD_SKIP_UNDERFLOW) && (flags & (ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP)))
         return ALIBI_ERR_INVALID;
+    // the skip bound follows the causal range (tiles left of the diagonal)
+    if ((flags & ALIBI_FWD_SKIP_UNDERFLOW) && !causal) return ALIBI_ERR_UNSUPPORTED;
+    if (opt->slopes && !slopes_ok(H, opt->slopes)) return ALIBI_ERR_INVALID;
     Slopes s;
-    fill_slopes(H, &s);
-    return to_status(launch_fwd_tc(q, k, v, out, lse, B, H, N, d, flags, clamp_min, softcap_z, s,
+    if (opt->slopes)
+        fill_slopes_from(H, opt->slopes, &s);
+    else
+        fill_slopes(H, &s);
+    return to_status(launch_fwd_tc(q, k, v, out, lse, B, H, N, d, causal, flags, clamp_min, softcap_z, s,
                                    static_cast<cudaStream_t>(stream)));
 }
 
@@ -255,11 +298,10 @@ int alibi_attn_fwd_f32(const float *q, const float *k, const float *v, float *ou
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
     if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
-    if (causal == 0) return ALIBI_ERR_UNSUPPORTED;
     if (d > 256) return ALIBI_ERR_UNSUPPORTED;
     Slopes s;
     fill_slopes(H, &s);
-    return to_status(launch_fwd_f32(q, k, v, out, lse, B, H, N, d, s, static_cast<cudaStream_t>(stream)));
+    return to_status(launch_fwd_f32(q, k, v, out, lse, B, H, N, d, causal, s, static_cast<cudaStream_t>(stream)));
 }
 
 int alibi_attn_decode(const void *q, const void *kcache, const void *vcache, void *out, int B, int H, int L, int d,
@@ -286,13 +328,20 @@ int alibi_attn_decode_splits(int B, int H, int L, int d)
 int alibi_attn_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N, int d,
                          void *stream)
 {
+    return alibi_attn_probs_f32_ex(q, k, lse, P, B, H, N, d, 1, stream);
+}
+
+int alibi_attn_probs_f32_ex(const float *q, const float *k, const float *lse, float *P, int B, int H, int N, int d,
+                            int causal, void *stream)
+{
     if (!q || !k || !lse || !P) return ALIBI_ERR_INVALID;
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
+    if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
     if (d > 256) return ALIBI_ERR_UNSUPPORTED;
     Slopes s;
     fill_slopes(H, &s);
-    return to_status(launch_probs_f32(q, k, lse, P, B, H, N, d, s, static_cast<cudaStream_t>(stream)));
+    return to_status(launch_probs_f32(q, k, lse, P, B, H, N, d, causal, s, static_cast<cudaStream_t>(stream)));
 }
 
 int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N, int d, float tau,

@@ -1,6 +1,8 @@
 // CUDA-core kernels of the library:
-//   - fp32 causal prefill at reference precision (IEEE expf/logf), one warp
-//     per query row, keys processed 32 at a time with an online softmax;
+//   - fp32 prefill at reference precision (IEEE expf/logf), one warp per
+//     query row, keys processed 32 at a time with an online softmax; causal,
+//     or over all keys with the symmetric distance |i - j| ("ALiBi and
+//     Relative Position Bias", "The mechanics");
 //   - export of the fp32 attention weights from the saved LSE;
 //   - the bf16 underflow counter: per head, the number of causal pairs whose
 //     max-subtracted exponent is <= tau, in two passes per row (row max, then
@@ -46,7 +48,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) fwd_f32_kernel(const float
                                                                       const float *__restrict__ k,
                                                                       const float *__restrict__ v, float *__restrict__ out,
                                                                       float *__restrict__ lse, long long rows, int H,
-                                                                      int N, int d, float scale, Slopes slopes)
+                                                                      int N, int d, int causal, float scale,
+                                                                      Slopes slopes)
 {
     __shared__ float qsm[kRowsPerBlock][32 * DPL];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -63,17 +66,19 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) fwd_f32_kernel(const float
     float m = -INFINITY, l = 0.f, o[DPL];
 #pragma unroll
     for (int u = 0; u < DPL; ++u) o[u] = 0.f;
-    for (int j0 = 0; j0 <= i; j0 += 32) {
+    const int jlast = causal ? i : N - 1;  // last key the row attends to
+    for (int j0 = 0; j0 <= jlast; j0 += 32) {
         const int j = j0 + lane;
-        const float x = (j <= i) ? f32_logit(qsm[warp], kb + static_cast<long long>(j) * d, d, scale, slope, i - j)
-                                 : -INFINITY;
-        const float mn = fmaxf(m, warp_max(x));  // finite: key j0 <= i is always allowed
+        const float x = (j <= jlast) ? f32_logit(qsm[warp], kb + static_cast<long long>(j) * d, d, scale, slope,
+                                                 abs(i - j))
+                                     : -INFINITY;
+        const float mn = fmaxf(m, warp_max(x));  // finite: key j0 <= jlast is always allowed
         const float alpha = expf(m - mn);        // 0 on the first block (m = -inf)
-        const float pj = (j <= i) ? expf(x - mn) : 0.f;
+        const float pj = (j <= jlast) ? expf(x - mn) : 0.f;
         l = l * alpha + warp_sum(pj);
 #pragma unroll
         for (int u = 0; u < DPL; ++u) o[u] *= alpha;
-        const int jn = min(32, i - j0 + 1);
+        const int jn = min(32, jlast - j0 + 1);
         for (int jj = 0; jj < jn; ++jj) {
             const float pb = __shfl_sync(0xffffffffu, pj, jj);
             const float *vr = vb + static_cast<long long>(j0 + jj) * d;
@@ -93,10 +98,11 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) fwd_f32_kernel(const float
     if (lse && lane == 0) lse[row] = m + logf(l);
 }
 
-// P[b,h,i,j] = exp(x_ij - lse_i) for j <= i, else 0. One thread per (row, j).
+// P[b,h,i,j] = exp(x_ij - lse_i) for every allowed key (j <= i when causal), else 0.
+// One thread per (row, j).
 __global__ void probs_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                                  const float *__restrict__ lse, float *__restrict__ P, long long total, int H, int N,
-                                 int d, float scale, Slopes slopes)
+                                 int d, int causal, float scale, Slopes slopes)
 {
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= total) return;
@@ -105,8 +111,8 @@ __global__ void probs_f32_kernel(const float *__restrict__ q, const float *__res
     const long long bh = row / N;
     const int i = static_cast<int>(row - bh * N);
     float pij = 0.f;
-    if (j <= i) {
-        const float x = f32_logit(q + row * d, k + (bh * N + j) * d, d, scale, slopes.nat[bh % H], i - j);
+    if (!causal || j <= i) {
+        const float x = f32_logit(q + row * d, k + (bh * N + j) * d, d, scale, slopes.nat[bh % H], abs(i - j));
         pij = expf(x - lse[row]);
     }
     P[idx] = pij;
@@ -206,7 +212,7 @@ cudaError_t launch_selftest_timeout(cudaStream_t stream)
 }
 
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B, int H,
-                           int N, int d, const Slopes &slopes, cudaStream_t stream)
+                           int N, int d, int causal, const Slopes &slopes, cudaStream_t stream)
 {
     const long long rows = static_cast<long long>(B) * H * N;
     const unsigned grid = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
@@ -214,7 +220,8 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
     const int dpl = (d + 31) / 32;
 #define ALIBI_F32_CASE(X)                                                                                        \
     case X:                                                                                                      \
-        fwd_f32_kernel<X><<<grid, kRowsPerBlock * 32, 0, stream>>>(q, k, v, out, lse, rows, H, N, d, scale, slopes); \
+        fwd_f32_kernel<X><<<grid, kRowsPerBlock * 32, 0, stream>>>(q, k, v, out, lse, rows, H, N, d, causal, scale, \
+                                                                    slopes);                               \
         break;
     switch (dpl) {
         ALIBI_F32_CASE(1)
@@ -233,13 +240,13 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
 }
 
 cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N, int d,
-                             const Slopes &slopes, cudaStream_t stream)
+                             int causal, const Slopes &slopes, cudaStream_t stream)
 {
     const long long total = static_cast<long long>(B) * H * N * N;
     const int threads = 256;
     const long long blocks = (total + threads - 1) / threads;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    probs_f32_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(q, k, lse, P, total, H, N, d,
+    probs_f32_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(q, k, lse, P, total, H, N, d, causal,
                                                                             1.0f / sqrtf(static_cast<float>(d)),
                                                                             slopes);
     return cudaGetLastError();

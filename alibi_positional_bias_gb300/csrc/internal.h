@@ -26,6 +26,7 @@ struct Slopes {
 // Host helpers (alibi_host.cu).
 uint32_t *device_status_word();  // per current device, 2 words
 void fill_slopes(int H, Slopes *s);
+void fill_slopes_from(int H, const float *nat, Slopes *s);  // caller-chosen slopes (natural-log units)
 int num_sms();                   // of the current device
 cudaMemPool_t decode_pool();     // library-owned stream-ordered pool of the current device
 // 3-D TMA map over a [dim2, dim1, dim0] bf16 tensor (dim0 fastest), box {box0, box1, 1},
@@ -55,12 +56,12 @@ cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, 
 
 // Kernel launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
-                          int N, int d, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
+                          int N, int d, int causal, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
                           cudaStream_t stream);
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B,
-                           int H, int N, int d, const Slopes &slopes, cudaStream_t stream);
+                           int H, int N, int d, int causal, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N,
-                             int d, const Slopes &slopes, cudaStream_t stream);
+                             int d, int causal, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
                           const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(cudaStream_t stream);

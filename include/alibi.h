@@ -72,7 +72,8 @@ ALIBI_API int alibi_slopes(int H, float *out_host);
  * q, k, v: device bf16 [B, H, N, d]; out: device bf16 [B, H, N, d];
  * lse: device fp32 [B, H, N] (may be NULL to skip it);
  * LSE_i = ln sum_{j<=i} exp(q_i.k_j/sqrt(d) - m_h (i - j)).
- * d in {64, 128}; N >= 1; causal must be 1 (0 returns ALIBI_ERR_UNSUPPORTED).
+ * d in {64, 128}; N >= 1; causal = 1 (0: symmetric bias over all keys, see
+ * alibi_attn_fwd_ex).
  * Runs the tcgen05/TMEM/TMA kernel: scores and P.V on the tensor cores with
  * fp32 accumulation; the bias is generated from tile coordinates and never
  * stored; online softmax in fp32; P rounded to bf16 for the P.V product.
@@ -87,28 +88,57 @@ ALIBI_API int alibi_attn_fwd(const void *q, const void *k, const void *v, void *
 #define ALIBI_FWD_SOFTCAP 8u        /* content score A* = z tanh(A / z), z = softcap_z      */
 
 /*
- * alibi_attn_fwd with options; flags = 0 is exactly alibi_attn_fwd.
+ * Options of alibi_attn_fwd_ex (plain C; pass NULL for the defaults).
+ */
+typedef struct alibi_fwd_options {
+    unsigned int flags;   /* ALIBI_FWD_* bits                                             */
+    float clamp_min;      /* ALIBI_FWD_CLAMP: bias floor in natural-log units, < 0         */
+    float softcap_z;      /* ALIBI_FWD_SOFTCAP: cap z > 0                                  */
+    const float *slopes;  /* optional HOST array of H per-head slopes (natural-log units,
+                             finite, >= 0; > 0 with ALIBI_FWD_SKIP_UNDERFLOW); NULL means
+                             alibi_slopes(H). alibi_slopes_explicit() builds the paper's
+                             robust / explicit schedules.                               */
+} alibi_fwd_options;
+
+/*
+ * alibi_attn_fwd with options; opt = NULL (or all-zero) is exactly alibi_attn_fwd.
+ * causal = 0 selects the symmetric bias -m_h |i - j| over all keys ("ALiBi and
+ * Relative Position Bias", "The mechanics"; the encoder models of "When
+ * Attention Goes Blind", Table 5).
  *
- * ALIBI_FWD_SKIP_UNDERFLOW: leave out the KV tiles at the far end of each
- * query block's causal range whose weights provably flush to zero ("When
- * Attention Goes Blind", sec. 3.2-3.3: past the blindness distance the
+ * ALIBI_FWD_SKIP_UNDERFLOW (causal only): leave out the KV tiles at the far end
+ * of each query block's causal range whose weights provably flush to zero
+ * ("When Attention Goes Blind", sec. 3.2-3.3: past the blindness distance the
  * exponent falls below the smallest normal number; sec. 5.2: steep heads act
  * as a sliding window). A pre-pass bounds every score by |q_i| max_j |k_j| and
  * the running max from below by the diagonal score; a tile is left out only if
  * every exponent in it is below -127 (base 2), where the kernel's
  * flush-to-zero exponential returns exactly 0. Output and LSE are therefore
- * bit-identical to flags = 0. The pre-pass reads Q and K once and takes a
- * small plan buffer (items x 16 bytes) from the library's stream-ordered pool.
+ * bit-identical to the same call without the flag. The pre-pass reads Q and K
+ * once and takes a small plan buffer (items x 16 bytes) from the library's
+ * stream-ordered pool.
  *
  * ALIBI_FWD_CLAMP / _LOGDIST / _SOFTCAP: the mitigations of "When Attention
  * Goes Blind", sec. 3.4 (the paper trains with clamp_min = -87, sec. 4.3, and
- * z = 50). clamp_min is in natural-log units and must be < 0; softcap_z > 0.
- * They cannot be combined with ALIBI_FWD_SKIP_UNDERFLOW (clamped or
- * log-scaled biases do not underflow). Unused float arguments are ignored.
+ * z = 50), in any combination. They cannot be combined with
+ * ALIBI_FWD_SKIP_UNDERFLOW (clamped or log-scaled biases do not underflow).
  */
 ALIBI_API int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse,
-                   int B, int H, int N, int d, int causal, unsigned int flags, float clamp_min,
-                   float softcap_z, void *stream);
+                   int B, int H, int N, int d, int causal, const alibi_fwd_options *opt, void *stream);
+
+/*
+ * Explicit ("robust") slopes, "When Attention Goes Blind" sec. 3.4 "Robust
+ * Slopes" and sec. 4.3: choose the slopes so the blindness distances
+ * delta_h = min{D : -m_h D* <= tau} spread geometrically from delta_first
+ * (head 0, steepest) to delta_last (head H-1): delta_h = delta_first
+ * (delta_last / delta_first)^(h / (H - 1)), m_h = -tau / delta_h with linear
+ * distances, or m_h = -tau / ln(delta_h + 1) with log-scaled distances (the
+ * E+L combination). tau < 0 is the underflow threshold in natural-log units
+ * (ln 2^-126 = -87.3365 reproduces the paper's tables). Host-only; writes H
+ * fp32 values (rounded to nearest) to out_host.
+ */
+ALIBI_API int alibi_slopes_explicit(int H, double delta_first, double delta_last, double tau, int log_distance,
+                   float *out_host);
 
 /*
  * The skip plan alone (analysis and tests): for each work item w = (b*H + h) *
@@ -123,7 +153,8 @@ ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, i
 /*
  * Causal prefill in fp32 (reference precision): all inputs, outputs and
  * arithmetic in fp32 on the CUDA cores with IEEE expf. Same layouts and
- * semantics as alibi_attn_fwd; d in [1, 256]; lse may be NULL.
+ * semantics as alibi_attn_fwd (causal = 0: symmetric bias); d in [1, 256];
+ * lse may be NULL.
  */
 ALIBI_API int alibi_attn_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                        int B, int H, int N, int d, int causal, void *stream);
@@ -178,6 +209,11 @@ ALIBI_API int alibi_attn_decode_noalloc(const void *q, const void *kcache, const
  */
 ALIBI_API int alibi_attn_probs_f32(const float *q, const float *k, const float *lse, float *P,
                          int B, int H, int N, int d, void *stream);
+
+/* alibi_attn_probs_f32 for either mask: causal = 0 uses exp(x_ij - lse_i) with the
+ * symmetric bias -m_h |i - j| for every key. */
+ALIBI_API int alibi_attn_probs_f32_ex(const float *q, const float *k, const float *lse, float *P,
+                         int B, int H, int N, int d, int causal, void *stream);
 
 /*
  * Underflow count ("When Attention Goes Blind", sec. 3.2-3.3): per head h,

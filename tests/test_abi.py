@@ -101,19 +101,29 @@ def test_fwd_argument_errors(lib):
     assert f(P, P, P, P, P, 1, 1, 0, 64, 1, None) == ab.ALIBI_ERR_INVALID
     assert f(MIS, P, P, P, P, 1, 1, 8, 64, 1, None) == ab.ALIBI_ERR_INVALID
     assert f(P, P, P, P, P, 1, 1, 8, 64, 2, None) == ab.ALIBI_ERR_INVALID
-    assert f(P, P, P, P, P, 1, 1, 8, 64, 0, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert f(P, P, P, P, P, 1, 1, 8, 32, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert f(P, P, P, P, P, 1, 300, 8, 64, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
 
 
+def _opt(flags=0, clamp=0.0, z=0.0, slopes=None):
+    m = None if slopes is None else np.ascontiguousarray(slopes, dtype=np.float32)
+    o = ab.AlibiFwdOptions(flags, clamp, z, None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return ctypes.byref(o), m  # keep m alive with the struct
+
+
 def test_fwd_ex_flags_and_plan_errors(lib):
-    f = lib.alibi_attn_fwd_ex
-    U, F = ctypes.c_uint, ctypes.c_float
-    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(16), F(0), F(0), None) == ab.ALIBI_ERR_INVALID
-    assert f(P, P, P, P, P, 1, 1, 8, 32, 1, U(1), F(0), F(0), None) == ab.ALIBI_ERR_UNSUPPORTED
-    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(2), F(1.0), F(0), None) == ab.ALIBI_ERR_INVALID   # clamp >= 0
-    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(8), F(0), F(-5.0), None) == ab.ALIBI_ERR_INVALID  # z <= 0
-    assert f(P, P, P, P, P, 1, 1, 8, 64, 1, U(1 | 4), F(0), F(0), None) == ab.ALIBI_ERR_INVALID  # skip + logdist
+    def f(H, d, causal, *opt):
+        o, keep = _opt(*opt)
+        return lib.alibi_attn_fwd_ex(P, P, P, P, P, 1, H, 8, d, causal, o, None)
+    assert f(1, 64, 1, 16) == ab.ALIBI_ERR_INVALID                      # unknown flag
+    assert f(1, 32, 1, 1) == ab.ALIBI_ERR_UNSUPPORTED                   # head size
+    assert f(1, 64, 1, 2, 1.0) == ab.ALIBI_ERR_INVALID                  # clamp >= 0
+    assert f(1, 64, 1, 8, 0.0, -5.0) == ab.ALIBI_ERR_INVALID            # z <= 0
+    assert f(1, 64, 1, 1 | 4) == ab.ALIBI_ERR_INVALID                   # skip + logdist
+    assert f(1, 64, 0, 1) == ab.ALIBI_ERR_UNSUPPORTED                   # skip needs the causal range
+    assert f(2, 64, 1, 0, 0.0, 0.0, [0.5, -0.25]) == ab.ALIBI_ERR_INVALID         # negative slope
+    assert f(2, 64, 1, 0, 0.0, 0.0, [0.5, float("nan")]) == ab.ALIBI_ERR_INVALID  # non-finite slope
+    assert f(2, 64, 1, 0, 0.0, 0.0, [0.5, float("inf")]) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 64, None, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 48, P, None) == ab.ALIBI_ERR_UNSUPPORTED
 
@@ -124,7 +134,25 @@ def test_decode_and_aux_argument_errors(lib):
     assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 8, 64, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_fwd_f32(P, P, P, P, P, 1, 1, 8, 512, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_probs_f32(P, P, None, P, 1, 1, 8, 16, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_probs_f32_ex(P, P, P, P, 1, 1, 8, 16, 2, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_fwd_f32(P, P, P, P, P, 1, 1, 8, 16, 3, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_underflow_bf16(P, P, 1, 1, 8, 48, ctypes.c_float(-87.0), P, None) == \
         ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_underflow_bf16(P, P, 1, 1, 8, 64, ctypes.c_float(float("nan")), P, None) == \
         ab.ALIBI_ERR_INVALID
+
+
+def test_explicit_slopes_bit_exact_vs_oracle(lib):
+    # host-only: the library's robust-slope schedule against the oracle's, rounded once
+    import oracle
+    for H, d1, dH, logd in [(9, 128, 512, False), (9, 2048, 4096, False), (9, 16, 4096, False),
+                            (9, 32, 8192, False), (9, 32, 8192, True), (7, 32, 2048, False), (1, 100, 5000, False),
+                            (64, 10, 1e6, True), (256, 3, 3e5, False)]:
+        got = ab.alibi_slopes_explicit(H, d1, dH, log_distance=logd)
+        want = oracle.slopes_explicit(H, d1, dH, log_distance=logd).astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (H, d1, dH, logd)
+    for bad in [(0, 16, 64), (4, 0, 64), (4, 16, float("nan")), (4, 16, -1.0)]:
+        with pytest.raises(ab.AlibiError):
+            ab.alibi_slopes_explicit(*bad)
+    with pytest.raises(ab.AlibiError):
+        ab.alibi_slopes_explicit(4, 16, 64, tau=0.0)
