@@ -73,7 +73,7 @@ def load(build_if_missing: bool = False):
                                               ctypes.POINTER(F)]
         lib.alibi_attn_probs_f32_ex.argtypes = [vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_fwd_ex.restype = I
-        lib.alibi_attn_skip_plan.argtypes = [vp, vp, I, I, I, I, vp, vp]
+        lib.alibi_attn_skip_plan.argtypes = [vp, vp, I, I, I, I, ctypes.POINTER(F), vp, vp]
         lib.alibi_attn_skip_plan.restype = I
         lib.alibi_attn_decode.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
         lib.alibi_attn_probs_f32.argtypes = [vp, vp, vp, vp, I, I, I, I, vp]
@@ -222,7 +222,7 @@ def alibi_slopes_explicit(H: int, delta_first: float, delta_last: float, tau: fl
     return out
 
 
-def alibi_attn_skip_plan(q, k, first_tile=None, stream=None):
+def alibi_attn_skip_plan(q, k, first_tile=None, slopes=None, stream=None):
     """Per work item (b*H + h, 256-row block): the first 128-key tile the skipping
     prefill computes. Returns an int32 CUDA tensor [B*H*ceil(N/256)]."""
     import torch
@@ -233,7 +233,12 @@ def alibi_attn_skip_plan(q, k, first_tile=None, stream=None):
     if first_tile is None:
         first_tile = torch.empty(items, dtype=torch.int32, device=q.device)
     _need(first_tile, torch.int32, (items,), "first_tile")
-    _check(load().alibi_attn_skip_plan(_ptr(q), _ptr(k), B, H, N, d, _ptr(first_tile), _stream(stream, q.device)),
+    m = None if slopes is None else np.ascontiguousarray(slopes, dtype=np.float32)
+    if m is not None and m.shape != (H,):
+        raise ValueError(f"slopes: expected shape ({H},), got {m.shape}")
+    _check(load().alibi_attn_skip_plan(_ptr(q), _ptr(k), B, H, N, d,
+                                       None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                       _ptr(first_tile), _stream(stream, q.device)),
            "alibi_attn_skip_plan")
     return first_tile
 

@@ -265,15 +265,20 @@ int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, fl
                                    static_cast<cudaStream_t>(stream)));
 }
 
-int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, int *first_tile, void *stream)
+int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const float *slopes,
+                         int *first_tile, void *stream)
 {
     if (!q || !k || !first_tile) return ALIBI_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(first_tile) & 3u)) return ALIBI_ERR_INVALID;
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
     if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (slopes && !slopes_ok(H, slopes)) return ALIBI_ERR_INVALID;
     Slopes s;
-    fill_slopes(H, &s);
+    if (slopes)
+        fill_slopes_from(H, slopes, &s);
+    else
+        fill_slopes(H, &s);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int NQB = ((N + 127) / 128 + 1) / 2, items = B * H * NQB;
     void *ws = nullptr;

@@ -325,38 +325,65 @@ def run_native(args):
             dist.destroy_process_group()
         return
 
-    # -------------------- exact underflow-tile skipping (NEXT-2), same inputs, own timing
-    skip = None
-    if do_pre:
-        plan = ab.alibi_attn_skip_plan(q, k).cpu().numpy()
+    def timed_ms(fn) -> float:
+        """Per-launch device time (ms) of fn on `stream`: warm-up, L2 flush before each
+        launch outside the events, max over ranks."""
+        for _ in range(args.warmup):
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for s_i in range(K):
+            flush.fill_(1.0)
+            ev[s_i][0].record(stream)
+            fn()
+            ev[s_i][1].record(stream)
+        torch.cuda.synchronize()
+        t = torch.tensor([sum(e[0].elapsed_time(e[1]) for e in ev)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ab.alibi_check_error(stream)
+        return float(t[0]) / K
+
+    def tiles_kept(plan):
+        """(tiles the skipping kernel computes, causal tiles in all) from a skip plan."""
         NQB, NQT = (wp.N + 255) // 256, (wp.N + 127) // 128
-        tiles_all = tiles_run = 0
+        all_, run = 0, 0
         for w_i, first in enumerate(plan):
             qb = w_i % NQB
             for qt in (2 * qb, 2 * qb + 1):
                 if qt < NQT:
-                    tiles_all += qt + 1
-                    tiles_run += qt + 1 - min(int(first), qt + 1)
-        for _ in range(args.warmup):
-            ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for s_i in range(args.steps):
-            flush.fill_(1.0)
-            ev[s_i][0].record(stream)
-            ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True)
-            ev[s_i][1].record(stream)
-        torch.cuda.synchronize()
-        t_skip = torch.tensor([sum(e[0].elapsed_time(e[1]) for e in ev)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t_skip, op=dist.ReduceOp.MAX)
-        t_skip = float(t_skip[0]) / args.steps
-        tile_flops = 4.0 * 128 * 128 * wp.d  # QK^T + PV of one 128 x 128 tile
+                    all_ += qt + 1
+                    run += qt + 1 - min(int(first), qt + 1)
+        return run, all_
+
+    tile_flops = 4.0 * 128 * 128 * wp.d  # QK^T + PV of one 128 x 128 tile
+    # -------------------- exact underflow-tile skipping, same inputs, own timing
+    skip = noncausal = steep = None
+    if do_pre:
+        tiles_run, tiles_all = tiles_kept(ab.alibi_attn_skip_plan(q, k).cpu().numpy())
+        t_skip = timed_ms(lambda: ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True))
         skip = {"ms": t_skip, "launches": 4,  # key norms, item plan, plan sort, prefill
                 "algorithmic_tflops": world * prefill_flops(wp) / (t_skip / 1e3) / 1e12,
                 "executed_tflops": world * tiles_run * tile_flops / (t_skip / 1e3) / 1e12,
                 "tiles_skipped_frac": 1.0 - tiles_run / tiles_all,
                 "exact": "bit-identical to the dense kernel (tested)"}
-        ab.alibi_check_error(stream)
+
+        # -------------------- symmetric bias over all keys (causal = 0): 4 B H N^2 d flops
+        t_nc = timed_ms(lambda: ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, causal=False, stream=stream))
+        nc_tf = 2.0 * prefill_flops(wp) / (t_nc / 1e3) / 1e12
+        noncausal = {"ms": t_nc, "tflops": world * nc_tf, "unit": "TFLOP/s",
+                     "frac": nc_tf / peaks["bf16_tflops"], "peak_source": f"bf16 dense burst, {peaks['source']}"}
+
+        # -------------------- Steep robust-slope schedule (Table 8 targets 128..512), dense vs skipping
+        m_steep = ab.alibi_slopes_explicit(wp.H, 128, 512)
+        run_s, all_s = tiles_kept(ab.alibi_attn_skip_plan(q, k, slopes=m_steep).cpu().numpy())
+        t_sd = timed_ms(lambda: ab.alibi_attn_fwd_ex(q, k, v, out=out, lse=lse, slopes=m_steep, stream=stream))
+        t_ss = timed_ms(lambda: ab.alibi_attn_fwd_ex(q, k, v, out=out, lse=lse, flags=1, slopes=m_steep,
+                                                     stream=stream))
+        steep = {"schedule": f"blindness distances 128..512 geometric over {wp.H} heads",
+                 "dense_ms": t_sd, "skip_ms": t_ss, "speedup": t_sd / t_ss,
+                 "tiles_skipped_frac": 1.0 - run_s / all_s,
+                 "algorithmic_tflops_skip": world * prefill_flops(wp) / (t_ss / 1e3) / 1e12,
+                 "executed_tflops_skip": world * run_s * tile_flops / (t_ss / 1e3) / 1e12}
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
@@ -474,6 +501,8 @@ def run_native(args):
         },
         "underflow": underflow,
         "prefill_skip_underflow": skip,
+        "prefill_noncausal": noncausal,
+        "prefill_steep_slopes": steep,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,

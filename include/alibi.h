@@ -145,10 +145,11 @@ ALIBI_API int alibi_slopes_explicit(int H, double delta_first, double delta_last
  * ceil(N/256) + blk (query rows [256 blk, 256 blk + 256) of head (b, h)),
  * first_tile[w] is the first 128-key tile the skipping kernel computes; tiles
  * 0 .. first_tile[w]-1 are left out. first_tile: device int32 [B*H*ceil(N/256)].
- * d in {64, 128}.
+ * slopes: optional HOST array of H slopes as in alibi_fwd_options (NULL:
+ * alibi_slopes(H)). d in {64, 128}.
  */
-ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, int *first_tile,
-                   void *stream);
+ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const float *slopes,
+                   int *first_tile, void *stream);
 
 /*
  * Causal prefill in fp32 (reference precision): all inputs, outputs and

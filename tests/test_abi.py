@@ -124,8 +124,10 @@ def test_fwd_ex_flags_and_plan_errors(lib):
     assert f(2, 64, 1, 0, 0.0, 0.0, [0.5, -0.25]) == ab.ALIBI_ERR_INVALID         # negative slope
     assert f(2, 64, 1, 0, 0.0, 0.0, [0.5, float("nan")]) == ab.ALIBI_ERR_INVALID  # non-finite slope
     assert f(2, 64, 1, 0, 0.0, 0.0, [0.5, float("inf")]) == ab.ALIBI_ERR_INVALID
-    assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 64, None, None) == ab.ALIBI_ERR_INVALID
-    assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 48, P, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 64, None, None, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_skip_plan(P, P, 1, 1, 8, 48, None, P, None) == ab.ALIBI_ERR_UNSUPPORTED
+    neg = (ctypes.c_float * 2)(0.5, -1.0)
+    assert lib.alibi_attn_skip_plan(P, P, 1, 2, 8, 64, neg, P, None) == ab.ALIBI_ERR_INVALID
 
 
 def test_decode_and_aux_argument_errors(lib):
