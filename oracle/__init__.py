@@ -67,6 +67,8 @@ def _load():
         lib.oracle_bias_ex.restype = D
         lib.oracle_attn_rows.argtypes = [f32p, f32p, f32p, f64p, I, I, I, I, I, I, D, D, i64p,
                                          ctypes.c_long, f64p, f64p, f64p, I]
+        lib.oracle_attn_bwd.argtypes = [f32p, f32p, f32p, f32p, f64p, I, I, I, I, I, I, D, D, f64p, f64p, f64p,
+                                        f64p, f64p, I]
         lib.oracle_attn_decode.argtypes = [f32p, f32p, f32p, f64p, I, I, I, I, f64p, f64p, I]
         lib.oracle_underflow_rows.argtypes = [f32p, f32p, f64p, I, I, I, I, D, D, i64p, ctypes.c_long,
                                               u64p, u64p, I]
@@ -164,6 +166,23 @@ def attention(q, k, v, m=None, causal=True, rows=None, want_weights=False, varia
         if w is not None:
             w = w.reshape(B, H, N, N)
     return out, lse, w
+
+
+def attention_bwd(q, k, v, dout, m=None, causal=True, variant=0, c_clamp=-87.0, z_cap=50.0, nthreads=0):
+    """Oracle gradients (dq, dk, dv) [B, H, N, d] of sum(dout * attention(q, k, v)),
+    plus the per-row LSE and sum_j w_ij (dout_i . v_j) [B, H, N]."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, H, N, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and dout.shape == q.shape
+    m = slopes(H) if m is None else np.ascontiguousarray(m, dtype=np.float64)
+    dq, dk, dv = (np.empty((B, H, N, d), dtype=np.float64) for _ in range(3))
+    lse, rowdot = np.empty((B, H, N), dtype=np.float64), np.empty((B, H, N), dtype=np.float64)
+    p64 = lambda a: _ptr(a, ctypes.c_double)  # noqa: E731
+    _check(_load().oracle_attn_bwd(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
+                                   _ptr(dout, ctypes.c_float), p64(m), B, H, N, d, int(bool(causal)), int(variant),
+                                   float(c_clamp), float(z_cap), p64(dq), p64(dk), p64(dv), p64(lse), p64(rowdot),
+                                   int(nthreads)))
+    return dq, dk, dv, lse, rowdot
 
 
 def decode(q, kcache, vcache, m=None, nthreads=0):

@@ -32,7 +32,9 @@
  *    symmetric |i - j| distance used when causal == 0.
  *
  * Every function is pinned by the tests in tests/test_oracle_pins.py against
- * values the pages print, closed forms, invariants and brute force.
+ * values the pages print, closed forms, invariants and brute force; the
+ * backward pass (oracle_attn_bwd) by tests/test_oracle_bwd_pins.py against
+ * finite differences of the forward and gradient identities.
  */
 #include <math.h>
 #include <pthread.h>
@@ -305,6 +307,153 @@ int oracle_attn_rows(const float *q, const float *k, const float *v, const doubl
             if (rows[r] < 0 || rows[r] >= total) return ORACLE_EINVAL;
     attn_ctx c = {q, k, v, m, B, H, N, d, causal, variant, c_clamp, z_cap, rows, out, lse, w};
     return run_rows(attn_row, &c, nrows, N, nthreads);
+}
+
+/* --------------------------------------------------------------- backward */
+
+/*
+ * Gradients of the attention above for an upstream gradient dO, written out
+ * from the definition (the forward of "When Attention Goes Blind" sec. 3.1
+ * eq. 1-4; its sec. 5.1 remarks that only nonzero weights carry gradient):
+ *
+ *   w_ij  = softmax_j(x_ij)                      (allowed keys only)
+ *   g_ij  = dO_i . v_j                           d loss / d w_ij
+ *   dx_ij = w_ij (g_ij - sum_t w_it g_it)        softmax Jacobian applied to g
+ *   da_ij = dx_ij                                (z (1 - tanh^2(a_ij / z)) / z
+ *                                                 factor with ORACLE_SOFTCAP)
+ *   dQ_i  = sum_j da_ij k_j / sqrt(d)
+ *   dK_j  = sum_i da_ij q_i / sqrt(d)
+ *   dV_j  = sum_i w_ij dO_i
+ *
+ * The bias has no trainable parameter, so it only enters through w. Three
+ * passes, each a plain loop: per query row the weights' normaliser and the
+ * sum_t w_it g_it; dQ per query row; dK and dV per key (column of w).
+ */
+typedef struct {
+    const float *q, *k, *v, *dout;
+    const double *m;
+    int B, H, N, d, causal, variant;
+    double c_clamp, z_cap;
+    double *lse, *rowdot; /* per (b, h, i): ln sum_j e^{x_ij}, sum_j w_ij g_ij */
+    double *dq, *dk, *dv;
+} bwd_ctx;
+
+/* Logit x_ij of the forward (with its variants); -inf for masked keys. If araw
+ * is given it receives the scaled content score a_ij before soft capping. */
+static double bwd_logit(const bwd_ctx *c, long bh, long i, long j, double *araw)
+{
+    const size_t base = (size_t)bh * (size_t)c->N * (size_t)c->d;
+    double b = oracle_bias_ex(c->m[bh % c->H], i, j, c->causal, c->variant, c->c_clamp);
+    if (b == -INFINITY) return -INFINITY;
+    double a = content_score(c->q + base + (size_t)i * c->d, c->k + base + (size_t)j * c->d, c->d);
+    if (araw) *araw = a;
+    if (c->variant & ORACLE_SOFTCAP) a = softcap(a, c->z_cap);
+    return a + b;
+}
+
+static double bwd_g(const bwd_ctx *c, long bh, long i, long j)
+{
+    const size_t base = (size_t)bh * (size_t)c->N * (size_t)c->d;
+    const float *o = c->dout + base + (size_t)i * c->d, *vj = c->v + base + (size_t)j * c->d;
+    double g = 0.0;
+    for (int t = 0; t < c->d; ++t) g += (double)o[t] * (double)vj[t];
+    return g;
+}
+
+/* d x_ij / d a_ij: 1, or 1 - tanh^2(a / z) under soft capping. */
+static double bwd_cap_factor(const bwd_ctx *c, double a)
+{
+    if (!(c->variant & ORACLE_SOFTCAP)) return 1.0;
+    double t = tanh(a / c->z_cap);
+    return 1.0 - t * t;
+}
+
+/* pass 1, per query row: normaliser (as an LSE) and sum_t w_it g_it */
+static void bwd_row_stats(void *vctx, long r, double *x)
+{
+    const bwd_ctx *c = (const bwd_ctx *)vctx;
+    long bh = r / c->N, i = r % c->N;
+    double M = -INFINITY;
+    for (long j = 0; j < c->N; ++j) {
+        x[j] = bwd_logit(c, bh, i, j, NULL);
+        if (x[j] > M) M = x[j];
+    }
+    double Z = 0.0;
+    for (long j = 0; j < c->N; ++j) Z += exp(x[j] - M);
+    double s = 0.0;
+    for (long j = 0; j < c->N; ++j)
+        if (x[j] != -INFINITY) s += exp(x[j] - M) / Z * bwd_g(c, bh, i, j);
+    c->lse[r] = M + log(Z);
+    c->rowdot[r] = s;
+}
+
+/* pass 2, per query row: dQ_i */
+static void bwd_dq_row(void *vctx, long r, double *x)
+{
+    (void)x;
+    const bwd_ctx *c = (const bwd_ctx *)vctx;
+    long bh = r / c->N, i = r % c->N;
+    const size_t base = (size_t)bh * (size_t)c->N * (size_t)c->d;
+    double *dq = c->dq + (size_t)r * c->d;
+    for (int t = 0; t < c->d; ++t) dq[t] = 0.0;
+    for (long j = 0; j < c->N; ++j) {
+        double a = 0.0, xij = bwd_logit(c, bh, i, j, &a);
+        if (xij == -INFINITY) continue;
+        double w = exp(xij - c->lse[r]);
+        double da = w * (bwd_g(c, bh, i, j) - c->rowdot[r]) * bwd_cap_factor(c, a);
+        const float *kj = c->k + base + (size_t)j * c->d;
+        for (int t = 0; t < c->d; ++t) dq[t] += da * (double)kj[t];
+    }
+    for (int t = 0; t < c->d; ++t) dq[t] /= sqrt((double)c->d);
+}
+
+/* pass 3, per key (column): dK_j and dV_j */
+static void bwd_dkv_col(void *vctx, long r, double *x)
+{
+    (void)x;
+    const bwd_ctx *c = (const bwd_ctx *)vctx;
+    long bh = r / c->N, j = r % c->N;
+    const size_t base = (size_t)bh * (size_t)c->N * (size_t)c->d;
+    double *dk = c->dk + (size_t)r * c->d, *dv = c->dv + (size_t)r * c->d;
+    for (int t = 0; t < c->d; ++t) dk[t] = dv[t] = 0.0;
+    for (long i = 0; i < c->N; ++i) {
+        double a = 0.0, xij = bwd_logit(c, bh, i, j, &a);
+        if (xij == -INFINITY) continue;
+        long ri = bh * c->N + i;
+        double w = exp(xij - c->lse[ri]);
+        double da = w * (bwd_g(c, bh, i, j) - c->rowdot[ri]) * bwd_cap_factor(c, a);
+        const float *qi = c->q + base + (size_t)i * c->d, *oi = c->dout + base + (size_t)i * c->d;
+        for (int t = 0; t < c->d; ++t) {
+            dk[t] += da * (double)qi[t];
+            dv[t] += w * (double)oi[t];
+        }
+    }
+    for (int t = 0; t < c->d; ++t) dk[t] /= sqrt((double)c->d);
+}
+
+/*
+ * dq, dk, dv: B*H*N x d each (fp64). lse, rowdot: optional outputs of pass 1
+ * (B*H*N each); pass NULL to use internal buffers.
+ */
+int oracle_attn_bwd(const float *q, const float *k, const float *v, const float *dout, const double *m,
+                    int B, int H, int N, int d, int causal, int variant, double c_clamp, double z_cap,
+                    double *dq, double *dk, double *dv, double *lse, double *rowdot, int nthreads)
+{
+    if (!q || !k || !v || !dout || !m || !dq || !dk || !dv || B < 1 || H < 1 || N < 1 || d < 1)
+        return ORACLE_EINVAL;
+    long rows = (long)B * H * N;
+    double *l = lse ? lse : (double *)malloc(sizeof(double) * (size_t)rows);
+    double *rd = rowdot ? rowdot : (double *)malloc(sizeof(double) * (size_t)rows);
+    int st = ORACLE_ENOMEM;
+    if (l && rd) {
+        bwd_ctx c = {q, k, v, dout, m, B, H, N, d, causal, variant, c_clamp, z_cap, l, rd, dq, dk, dv};
+        st = run_rows(bwd_row_stats, &c, rows, N, nthreads);
+        if (st == ORACLE_OK) st = run_rows(bwd_dq_row, &c, rows, 1, nthreads);
+        if (st == ORACLE_OK) st = run_rows(bwd_dkv_col, &c, rows, 1, nthreads);
+    }
+    if (!lse) free(l);
+    if (!rowdot) free(rd);
+    return st;
 }
 
 /* ----------------------------------------------------------------- decode */

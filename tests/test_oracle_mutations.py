@@ -31,6 +31,18 @@ MUTANTS = [
     ("logdist_no_plus1", "D = log(D + 1.0);", "D = log(D);"),
     ("clamp_min", "if ((variant & ORACLE_CLAMP) && B < c_clamp) B = c_clamp;",
      "if ((variant & ORACLE_CLAMP) && B > c_clamp) B = c_clamp;"),
+    # backward pass
+    ("bwd_dq_no_rowdot", "double da = w * (bwd_g(c, bh, i, j) - c->rowdot[r]) * bwd_cap_factor(c, a);",
+     "double da = w * bwd_g(c, bh, i, j) * bwd_cap_factor(c, a);"),
+    ("bwd_dk_unscaled", "for (int t = 0; t < c->d; ++t) dk[t] /= sqrt((double)c->d);", ""),
+    ("bwd_dv_uses_dx", "dv[t] += w * (double)oi[t];", "dv[t] += da * (double)oi[t];"),
+    ("bwd_cap_factor_sign", "return 1.0 - t * t;", "return 1.0 + t * t;"),
+    ("bwd_dk_with_k", "dk[t] += da * (double)qi[t];", "dk[t] += da * (double)c->k[base + (size_t)i * c->d + t];"),
+    ("bwd_g_value_row_i", "(size_t)i * c->d, *vj = c->v + base + (size_t)j * c->d;",
+     "(size_t)i * c->d, *vj = c->v + base + (size_t)i * c->d;"),
+    ("bwd_rowdot_unweighted", "s += exp(x[j] - M) / Z * bwd_g(c, bh, i, j);", "s += bwd_g(c, bh, i, j);"),
+    ("bwd_dq_uses_q", "const float *kj = c->k + base + (size_t)j * c->d;\n        for (int t = 0; t < c->d; ++t) dq",
+     "const float *kj = c->q + base + (size_t)j * c->d;\n        for (int t = 0; t < c->d; ++t) dq"),
 ]
 
 
@@ -43,7 +55,8 @@ def test_pins_reject_mutant(tmp_path, name, old, new):
     mut_so = tmp_path / f"{name}.so"
     oracle.compile_to(str(mut_c), str(mut_so))
     env = dict(os.environ, ALIBI_ORACLE_LIB=str(mut_so))
+    pins = "test_oracle_bwd_pins.py" if name.startswith("bwd_") else "test_oracle_pins.py"
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(HERE, "test_oracle_pins.py")],
+                        os.path.join(HERE, pins)],
                        env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
