@@ -23,7 +23,7 @@ __all__ = [
     "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
     "alibi_attn_fwd", "alibi_attn_fwd_ex", "alibi_attn_skip_plan", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
     "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc", "alibi_selftest_timeout",
-    "alibi_slopes_explicit", "alibi_attn_probs_f32_ex", "AlibiFwdOptions",
+    "alibi_slopes_explicit", "alibi_attn_probs_f32_ex", "AlibiFwdOptions", "alibi_attn_bwd", "alibi_attn_bwd_f32",
 ]
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
@@ -71,6 +71,9 @@ def load(build_if_missing: bool = False):
         lib.alibi_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, ctypes.POINTER(AlibiFwdOptions), vp]
         lib.alibi_slopes_explicit.argtypes = [I, ctypes.c_double, ctypes.c_double, ctypes.c_double, I,
                                               ctypes.POINTER(F)]
+        lib.alibi_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I,
+                                        ctypes.POINTER(AlibiFwdOptions), vp]
+        lib.alibi_attn_bwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_probs_f32_ex.argtypes = [vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_fwd_ex.restype = I
         lib.alibi_attn_skip_plan.argtypes = [vp, vp, I, I, I, I, ctypes.POINTER(F), vp, vp]
@@ -220,6 +223,48 @@ def alibi_slopes_explicit(H: int, delta_first: float, delta_last: float, tau: fl
                                         int(bool(log_distance)), out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))),
            "alibi_slopes_explicit")
     return out
+
+
+def alibi_attn_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, causal: bool = True, slopes=None,
+                   stream=None):
+    """bf16 backward on the tensor cores: (dq, dk, dv) of sum(dout * out) for the
+    forward's out and lse. All tensors [B, H, N, d] bf16 CUDA tensors, lse fp32."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, N, d = q.shape
+    for t, name in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, q.shape, name)
+    _need(lse, torch.float32, (B, H, N), "lse")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, torch.bfloat16, q.shape, name)
+    m = None
+    if slopes is not None:
+        m = np.ascontiguousarray(slopes, dtype=np.float32)
+        if m.shape != (H,):
+            raise ValueError(f"slopes: expected shape ({H},), got {m.shape}")
+    opt = AlibiFwdOptions(0, 0.0, 0.0, None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    _check(load().alibi_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, H, N, d, int(bool(causal)), ctypes.byref(opt),
+                                 _stream(stream, q.device)), "alibi_attn_bwd")
+    return dq, dk, dv
+
+
+def alibi_attn_bwd_f32(q, k, v, out, lse, dout, causal: bool = True, stream=None):
+    """fp32 backward (reference precision). All tensors fp32 CUDA tensors."""
+    import torch
+    _need(q, torch.float32, None, "q")
+    B, H, N, d = q.shape
+    for t, name in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.float32, q.shape, name)
+    _need(lse, torch.float32, (B, H, N), "lse")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    _check(load().alibi_attn_bwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                     _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), _stream(stream, q.device)),
+           "alibi_attn_bwd_f32")
+    return dq, dk, dv
 
 
 def alibi_attn_skip_plan(q, k, first_tile=None, slopes=None, stream=None):

@@ -1,0 +1,716 @@
+// ALiBi attention backward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Gradients of sum(dO * O) for O = softmax(x) V with
+//   x_ij = q_i.k_j / sqrt(d) - m_h (i - j)   (causal; keys j > i masked)
+//   x_ij = q_i.k_j / sqrt(d) - m_h |i - j|   (non-causal)
+// the forward of "When Attention Goes Blind: Numerical Failure in ALiBi
+// Positional Encodings" (arXiv 2608.03994) sec. 3.1 eq. 1-4 (its sec. 5.1 notes
+// that only weights that did not underflow carry gradient: here, as in the
+// forward, a weight whose base-2 exponent is below -126 is exactly zero). With
+// the forward's LSE the weights are recomputed tile by tile, never stored:
+//   P_ij  = exp(x_ij - LSE_i),   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,
+//   dS_ij = P_ij (dP_ij - D_i),
+//   dV = P^T dO,   dK = dS^T Q / sqrt(d),   dQ = dS K / sqrt(d).
+// The bias has no trainable parameter and enters only through P.
+//
+// Three launches, no atomics (the result is deterministic):
+//   bwd_prep_kernel   D_i = dO_i . O_i (fp32 from the bf16 tensors)
+//   bwd_dkdv_kernel   one work item per (b, h) and 128-key tile: K, V stay in
+//                     shared memory, Q / dO tiles stream through 2-stage rings;
+//                     S^T = K Q^T and dP^T = V dO^T in TMEM, then
+//                     dV += P^T dO and dK += dS^T Q with P^T, dS^T read from TMEM
+//   bwd_dq_kernel     one work item per (b, h) and 128-query tile: Q, dO stay,
+//                     K / V stream; S = Q K^T, dP = dO V^T, dQ += dS K
+// Roles as in the forward kernel: warp 0 TMA producer, warp 1 TMEM allocator
+// and single-thread MMA issuer, warps 4-7 / 8-11 two elementwise warpgroups
+// that split each tile's 128 columns in halves (TMEM lane = row of the tile).
+
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace alibi {
+namespace {
+
+constexpr int BT = 128;  // rows / columns of every tile
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kRegsLow = 88;
+constexpr uint32_t kRegsHigh = 208;
+static_assert(128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs, "register split must match launch");
+constexpr float kLog2e = 1.4426950408889634f;
+
+// TMEM columns (both main kernels): accumulators at 0 and 128 (dV, dK or dQ),
+// S / S^T at 256 (P or dS bf16 written over its halves), dP / dP^T at 384.
+constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColS = 256, kColP = 384;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr uint32_t kChunkBytes = BT * 128;
+    static constexpr uint32_t kTileBytes = BT * D * 2;
+    // dKdV: K, V resident; Q, dO rings. dQ: Q, dO resident; K, V rings. Same layout:
+    static constexpr uint32_t kRes0 = 0;                         // K (dKdV) / Q (dQ)
+    static constexpr uint32_t kRes1 = kTileBytes;                // V (dKdV) / dO (dQ)
+    static constexpr uint32_t kRing0 = 2 * kTileBytes;           // Q / K, 2 stages
+    static constexpr uint32_t kRing1 = 4 * kTileBytes;           // dO / V, 2 stages
+    static constexpr uint32_t kStats = 6 * kTileBytes;           // dKdV: per warp 2 x (64 + 64) floats
+    static constexpr uint32_t kBar = kStats + 8 * 2 * 128 * 4;
+    static constexpr uint32_t kSmem = kBar + 256 + 1024;
+};
+
+struct BwdParams {
+    CUtensorMap tq, tk, tv, tdo;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
+    const float *lse;             // [BH, N] natural log (forward output)
+    const float *dsum;            // [BH, N] D_i
+    __nv_bfloat16 *g0, *g1;       // dKdV: dk, dv; dQ: dq
+    uint32_t *err;
+    int N, BH, H, NT, num_items, causal;
+    float c1;       // log2(e) / sqrt(d)
+    float inv_sqrt_d;
+    Slopes slopes;
+};
+
+enum : uint32_t {
+    SITE_B_PROD_RES = 0x401, SITE_B_PROD_RING = 0x402, SITE_B_MMA_RES = 0x411, SITE_B_MMA_RING = 0x412,
+    SITE_B_MMA_P = 0x413, SITE_B_MMA_ACC = 0x414, SITE_B_MMA_DONE = 0x415, SITE_B_EW_S = 0x421,
+    SITE_B_EW_ACC = 0x422,
+};
+
+__device__ __forceinline__ int item_index(int k)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    return (k & 1) ? (k + 1) * G - 1 - c : k * G + c;
+}
+
+struct BItem {
+    int bh, tile, n;
+};
+
+// dKdV items: round r of the schedule is KV tile r of every (b, h) (causal: the
+// longest first, since tile jt meets NT - jt query tiles).
+__device__ __forceinline__ BItem dkdv_item(const BwdParams &p, int idx)
+{
+    BItem it;
+    const int round = idx / p.BH;
+    it.bh = idx - round * p.BH;
+    it.tile = round;
+    it.n = p.causal ? p.NT - round : p.NT;
+    return it;
+}
+
+// Query tile visited at iteration `it` of a dKdV item (causal: from the diagonal up).
+__device__ __forceinline__ int dkdv_qtile(const BwdParams &p, const BItem &t, int it)
+{
+    return p.causal ? t.tile + it : it;
+}
+
+// dQ items: round r is query tile NT - 1 - r of every (b, h) (causal: longest first).
+__device__ __forceinline__ BItem dq_item(const BwdParams &p, int idx)
+{
+    BItem it;
+    const int round = idx / p.BH;
+    it.bh = idx - round * p.BH;
+    it.tile = p.NT - 1 - round;
+    it.n = p.causal ? it.tile + 1 : p.NT;
+    return it;
+}
+
+// Descriptor helpers (128-byte swizzle, as the TMA writes it).
+// K-major operand (the contraction runs along d): 32-byte steps inside a swizzle
+// atom, one 16 KB atom per 64 columns of d.
+template <int D>
+__device__ __forceinline__ uint32_t kmajor_step(int kk)
+{
+    return ((kk >> 2) * BwdCfg<D>::kChunkBytes + (kk & 3) * 32) >> 4;
+}
+// MN-major operand (the contraction runs along the tile's rows): 16 rows = 2048 bytes per step.
+__device__ __forceinline__ uint32_t mnmajor_step(int kk) { return (kk * 2048) >> 4; }
+
+// A operand read from TMEM: bf16 pairs written by the two warpgroups over the
+// first 32 columns of their own 64-column halves of the S / dP region.
+__device__ __forceinline__ uint32_t tmem_a_col(uint32_t region, int kk)
+{
+    return region + 64 * (kk >> 2) + (kk & 3) * 8;
+}
+
+__device__ __forceinline__ void load_bf16_rows_store(__nv_bfloat16 *row, const uint32_t (&o)[32], float scale)
+{
+    uint32_t b[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+        b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * scale, __uint_as_float(o[2 * u + 1]) * scale);
+    uint4 *dst = reinterpret_cast<uint4 *>(row);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+}
+
+// Epilogue of one accumulator: this warpgroup's half of d for its thread's row.
+template <int D>
+__device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0, int s, __nv_bfloat16 *row,
+                                               bool valid, float scale)
+{
+    constexpr int kHalf = D / 2;
+#pragma unroll
+    for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + col0 + s * kHalf + c * 32, o);
+        tmem_wait_ld();
+        if (valid) load_bf16_rows_store(row + s * kHalf + c * 32, o, scale);
+    }
+}
+
+// ------------------------------------------------------------------ dK, dV
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBar);
+    uint64_t *kv_full = bars + 0;
+    uint64_t *kv_empty = bars + 1;
+    uint64_t *qo_full = bars + 2;   // [2]
+    uint64_t *qo_empty = bars + 4;  // [2]
+    uint64_t *s_full = bars + 6;
+    uint64_t *p_full = bars + 7;
+    uint64_t *acc_full = bars + 8;
+    uint64_t *acc_empty = bars + 9;
+    uint64_t *mma_done = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t *err = p.err;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qo_full[s], 1);
+            mbar_init(&qo_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 8);  // one arrival per elementwise warp
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tq);
+        tma_prefetch_desc(&p.tk);
+        tma_prefetch_desc(&p.tv);
+        tma_prefetch_desc(&p.tdo);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            uint32_t qc = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = item_index(k);
+                if (w >= p.num_items) break;
+                const BItem t = dkdv_item(p, w);
+                ok = mbar_wait(kv_empty, (k & 1) ^ 1, err, SITE_B_PROD_RES);
+                if (!ok) break;
+                mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(smem + C::kRes0 + c * C::kChunkBytes, &p.tk, 64 * c, t.tile * BT, t.bh, kv_full);
+                    tma_load_3d(smem + C::kRes1 + c * C::kChunkBytes, &p.tv, 64 * c, t.tile * BT, t.bh, kv_full);
+                }
+                for (int it = 0; it < t.n && ok; ++it, ++qc) {
+                    const uint32_t st = qc & 1, ph = (qc >> 1) & 1;
+                    ok = mbar_wait(&qo_empty[st], ph ^ 1, err, SITE_B_PROD_RING);
+                    if (!ok) break;
+                    const int qt = dkdv_qtile(p, t, it);
+                    mbar_arrive_expect_tx(&qo_full[st], 2 * C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(smem + C::kRing0 + st * C::kTileBytes + c * C::kChunkBytes, &p.tq, 64 * c,
+                                    qt * BT, t.bh, &qo_full[st]);
+                        tma_load_3d(smem + C::kRing1 + st * C::kTileBytes + c * C::kChunkBytes, &p.tdo, 64 * c,
+                                    qt * BT, t.bh, &qo_full[st]);
+                    }
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idS = idesc_bf16_f32(BT, BT, 0);
+            constexpr uint32_t idG = idesc_bf16_f32(BT, D, 1);
+            const uint32_t sK = smem_u32(smem + C::kRes0), sV = smem_u32(smem + C::kRes1);
+            const uint32_t sQ = smem_u32(smem + C::kRing0), sO = smem_u32(smem + C::kRing1);
+            const uint64_t kd = smem_desc_sw128(sK, 16, 1024), vd = smem_desc_sw128(sV, 16, 1024);
+            uint32_t qc = 0, pc = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = item_index(k);
+                if (w >= p.num_items) break;
+                const BItem t = dkdv_item(p, w);
+                ok = mbar_wait(kv_full, k & 1, err, SITE_B_MMA_RES);
+                if (!ok) break;
+                for (int it = 0; it < t.n && ok; ++it, ++qc) {
+                    const uint32_t st = qc & 1, ph = (qc >> 1) & 1;
+                    ok = mbar_wait(&qo_full[st], ph, err, SITE_B_MMA_RING);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // S^T = K Q^T and dP^T = V dO^T (both operands K-major along d)
+                    const uint64_t qd = smem_desc_sw128(sQ + st * C::kTileBytes, 16, 1024);
+                    const uint64_t od = smem_desc_sw128(sO + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + kColS, kd + kmajor_step<D>(kk), qd + kmajor_step<D>(kk), idS, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + kColP, vd + kmajor_step<D>(kk), od + kmajor_step<D>(kk), idS, kk > 0);
+                    mma_commit(s_full);
+                    // P^T and dS^T written back by the elementwise warps
+                    ok = mbar_wait(p_full, pc & 1, err, SITE_B_MMA_P);
+                    ++pc;
+                    if (ok && it == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // dV += P^T dO, dK += dS^T Q (B operands MN-major: the contraction runs over queries)
+                    const uint64_t omn = smem_desc_sw128(sO + st * C::kTileBytes, C::kChunkBytes, 1024);
+                    const uint64_t qmn = smem_desc_sw128(sQ + st * C::kTileBytes, C::kChunkBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), omn + mnmajor_step(kk), idG,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts(tmem + kColAcc1, tmem + tmem_a_col(kColP, kk), qmn + mnmajor_step(kk), idG,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&qo_empty[st]);
+                }
+                if (!ok) break;
+                mma_commit(kv_empty);
+                mma_commit(acc_full);
+            }
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE);
+        }
+    } else {
+        // --------------------------------------------------- elementwise warps
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        const int s = (warp - 4) >> 2;  // query columns [64 s, 64 s + 64) of every tile
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // key row of the tile
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        // per-warp double buffer of the 64 columns' LSE (base 2) and D
+        float *stats = reinterpret_cast<float *>(smem + C::kStats) + (warp - 4) * 2 * 128;
+        uint32_t s_cnt = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int w = item_index(k);
+            if (w >= p.num_items) break;
+            const BItem t = dkdv_item(p, w);
+            const float sl2 = p.slopes.log2e[t.bh % p.H];
+            const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
+            // this lane's share of the column statistics of iteration `it` (prefetched one ahead)
+            auto fetch = [&](int it, float (&v)[4]) {
+                const int q0 = dkdv_qtile(p, t, it) * BT + 64 * s;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i = q0 + lane + 32 * h;
+                    const bool in = i < p.N;
+                    v[h] = in ? p.lse[rowbase + i] * kLog2e : INFINITY;  // past N: weight 0
+                    v[2 + h] = in ? p.dsum[rowbase + i] : 0.f;
+                }
+            };
+            float pre[4];
+            fetch(0, pre);
+            for (int it = 0; it < t.n; ++it) {
+                const int qt = dkdv_qtile(p, t, it);
+                float *buf = stats + (it & 1) * 128;
+                buf[lane] = pre[0];
+                buf[lane + 32] = pre[1];
+                buf[64 + lane] = pre[2];
+                buf[64 + lane + 32] = pre[3];
+                __syncwarp();
+                if (it + 1 < t.n) fetch(it + 1, pre);
+                ok = mbar_wait(s_full, s_cnt & 1, err, SITE_B_EW_S);
+                ++s_cnt;
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sraw[64], draw[64];
+                tmem_ld32(lane_addr + kColS + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&sraw[0]));
+                tmem_ld32(lane_addr + kColS + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sraw[32]));
+                tmem_ld32(lane_addr + kColP + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&draw[0]));
+                tmem_ld32(lane_addr + kColP + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&draw[32]));
+                tmem_wait_ld();
+                // sl2 (i - j) for query i = qt*128 + 64 s + c and key j = jt*128 + r, from integers
+                const float base = sl2 * static_cast<float>((qt - t.tile) * BT + 64 * s - r);
+                const bool diag = p.causal && qt == t.tile;
+                uint32_t pk[32], dk[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int c = 2 * u + e;
+                        const float tt = fmaf(sl2, static_cast<float>(c), base);
+                        const float b = p.causal ? -tt : -fabsf(tt);
+                        float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) - buf[c];
+                        if (diag && 64 * s + c < r) x = -INFINITY;  // query before key: masked
+                        pv[e] = ex2_approx(x);
+                        dv[e] = pv[e] * (__uint_as_float(draw[c]) - buf[64 + c]);
+                    }
+                    pk[u] = pack_bf16x2(pv[0], pv[1]);
+                    dk[u] = pack_bf16x2(dv[0], dv[1]);
+                }
+                tmem_st32(lane_addr + kColS + 64 * s, pk);
+                tmem_st32(lane_addr + kColP + 64 * s, dk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+            }
+            if (!ok) break;
+            // ------------------------------------------------------ epilogue
+            ok = mbar_wait(acc_full, k & 1, err, SITE_B_EW_ACC);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int j = t.tile * BT + r;
+            const bool valid = j < p.N;
+            const size_t off = (rowbase + (valid ? j : 0)) * D;
+            store_acc_half<D>(lane_addr, kColAcc0, s, p.g1 + off, valid, 1.0f);           // dV
+            store_acc_half<D>(lane_addr, kColAcc1, s, p.g0 + off, valid, p.inv_sqrt_d);   // dK
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------- dQ
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBar);
+    uint64_t *qd_full = bars + 0;
+    uint64_t *qd_empty = bars + 1;
+    uint64_t *kv_full = bars + 2;   // [2]
+    uint64_t *kv_empty = bars + 4;  // [2]
+    uint64_t *s_full = bars + 6;
+    uint64_t *p_full = bars + 7;
+    uint64_t *acc_full = bars + 8;
+    uint64_t *acc_empty = bars + 9;
+    uint64_t *mma_done = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t *err = p.err;
+
+    if (threadIdx.x == 0) {
+        mbar_init(qd_full, 1);
+        mbar_init(qd_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 8);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tq);
+        tma_prefetch_desc(&p.tk);
+        tma_prefetch_desc(&p.tv);
+        tma_prefetch_desc(&p.tdo);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+        if (warp == 0 && lane == 0) {
+            uint32_t kc = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = item_index(k);
+                if (w >= p.num_items) break;
+                const BItem t = dq_item(p, w);
+                ok = mbar_wait(qd_empty, (k & 1) ^ 1, err, SITE_B_PROD_RES);
+                if (!ok) break;
+                mbar_arrive_expect_tx(qd_full, 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(smem + C::kRes0 + c * C::kChunkBytes, &p.tq, 64 * c, t.tile * BT, t.bh, qd_full);
+                    tma_load_3d(smem + C::kRes1 + c * C::kChunkBytes, &p.tdo, 64 * c, t.tile * BT, t.bh, qd_full);
+                }
+                for (int it = 0; it < t.n && ok; ++it, ++kc) {
+                    const uint32_t st = kc & 1, ph = (kc >> 1) & 1;
+                    ok = mbar_wait(&kv_empty[st], ph ^ 1, err, SITE_B_PROD_RING);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(smem + C::kRing0 + st * C::kTileBytes + c * C::kChunkBytes, &p.tk, 64 * c,
+                                    it * BT, t.bh, &kv_full[st]);
+                        tma_load_3d(smem + C::kRing1 + st * C::kTileBytes + c * C::kChunkBytes, &p.tv, 64 * c,
+                                    it * BT, t.bh, &kv_full[st]);
+                    }
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BT, BT, 0);
+            constexpr uint32_t idG = idesc_bf16_f32(BT, D, 1);
+            const uint32_t sQ = smem_u32(smem + C::kRes0), sO = smem_u32(smem + C::kRes1);
+            const uint32_t sK = smem_u32(smem + C::kRing0), sV = smem_u32(smem + C::kRing1);
+            const uint64_t qd = smem_desc_sw128(sQ, 16, 1024), od = smem_desc_sw128(sO, 16, 1024);
+            uint32_t kc = 0, pc = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int w = item_index(k);
+                if (w >= p.num_items) break;
+                const BItem t = dq_item(p, w);
+                ok = mbar_wait(qd_full, k & 1, err, SITE_B_MMA_RES);
+                if (!ok) break;
+                for (int it = 0; it < t.n && ok; ++it, ++kc) {
+                    const uint32_t st = kc & 1, ph = (kc >> 1) & 1;
+                    ok = mbar_wait(&kv_full[st], ph, err, SITE_B_MMA_RING);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // S = Q K^T and dP = dO V^T
+                    const uint64_t kd = smem_desc_sw128(sK + st * C::kTileBytes, 16, 1024);
+                    const uint64_t vd = smem_desc_sw128(sV + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + kColS, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idS, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + kColP, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idS, kk > 0);
+                    mma_commit(s_full);
+                    ok = mbar_wait(p_full, pc & 1, err, SITE_B_MMA_P);
+                    ++pc;
+                    if (ok && it == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // dQ += dS K (K MN-major: the contraction runs over keys)
+                    const uint64_t kmn = smem_desc_sw128(sK + st * C::kTileBytes, C::kChunkBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), kmn + mnmajor_step(kk), idG,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&kv_empty[st]);
+                }
+                if (!ok) break;
+                mma_commit(qd_empty);
+                mma_commit(acc_full);
+            }
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE);
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        const int s = (warp - 4) >> 2;  // key columns [64 s, 64 s + 64) of every tile
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // query row of the tile
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        uint32_t s_cnt = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int w = item_index(k);
+            if (w >= p.num_items) break;
+            const BItem t = dq_item(p, w);
+            const float sl2 = p.slopes.log2e[t.bh % p.H];
+            const int i = t.tile * BT + r;
+            const bool valid = i < p.N;
+            const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
+            const float lse2 = valid ? p.lse[rowbase + i] * kLog2e : 0.f;
+            const float Di = valid ? p.dsum[rowbase + i] : 0.f;
+            for (int it = 0; it < t.n; ++it) {
+                ok = mbar_wait(s_full, s_cnt & 1, err, SITE_B_EW_S);
+                ++s_cnt;
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sraw[64], draw[64];
+                tmem_ld32(lane_addr + kColS + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&sraw[0]));
+                tmem_ld32(lane_addr + kColS + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sraw[32]));
+                tmem_ld32(lane_addr + kColP + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&draw[0]));
+                tmem_ld32(lane_addr + kColP + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&draw[32]));
+                tmem_wait_ld();
+                // -sl2 (i - k) for key k = it*128 + 64 s + c, from the integer offset
+                const float nb = -sl2 * static_cast<float>(i - it * BT - 64 * s);
+                const bool diag = p.causal && it == t.tile;
+                const float nl = -lse2;
+                uint32_t dk[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    float dv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int c = 2 * u + e;
+                        const float tt = fmaf(sl2, static_cast<float>(c), nb);
+                        const float b = p.causal ? tt : -fabsf(tt);
+                        float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) + nl;
+                        if (diag && 64 * s + c > r) x = -INFINITY;  // key after the query: masked
+                        const float pv = ex2_approx(x);
+                        dv[e] = pv * (__uint_as_float(draw[c]) - Di);
+                    }
+                    dk[u] = pack_bf16x2(dv[0], dv[1]);
+                }
+                tmem_st32(lane_addr + kColS + 64 * s, dk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+            }
+            if (!ok) break;
+            ok = mbar_wait(acc_full, k & 1, err, SITE_B_EW_ACC);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            store_acc_half<D>(lane_addr, kColAcc0, s, p.g0 + (rowbase + (valid ? i : 0)) * D, valid, p.inv_sqrt_d);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- D = dO . O
+
+// One half-warp per row (8 bf16 per lane), D / 8 lanes per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ out,
+                                                       const __nv_bfloat16 *__restrict__ dout,
+                                                       float *__restrict__ dsum, long long rows)
+{
+    constexpr int LPR = D / 8, RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const long long row = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW + lane / LPR;
+    const int l = lane % LPR;
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(out + row * D + 8 * l);
+        const uint4 b = *reinterpret_cast<const uint4 *>(dout + row * D + 8 * l);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            acc = fmaf(__uint_as_float(wa[t] << 16), __uint_as_float(wb[t] << 16), acc);
+            acc = fmaf(__uint_as_float(wa[t] & 0xFFFF0000u), __uint_as_float(wb[t] & 0xFFFF0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int o = LPR / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (row < rows && l == 0) dsum[row] = acc;
+}
+
+template <typename K>
+cudaError_t check_launch_regs(K kernel, uint32_t smem)
+{
+    // The register split only balances if the kernel launches with exactly kLaunchRegs per
+    // thread; refuse to launch otherwise (an unbalanced setmaxnreg.inc would never return).
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                         const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int causal,
+                         const Slopes &slopes, float *dsum, cudaStream_t stream)
+{
+    using C = BwdCfg<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = check_launch_regs(bwd_dkdv_kernel<D>, C::kSmem);
+        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D>, C::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const long long rows = static_cast<long long>(B) * H * N;
+    constexpr int kRowsPerCta = 8 * (32 / (D / 8));
+    bwd_prep_kernel<D><<<static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), dsum, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    BwdParams p;
+    const uint64_t BH = static_cast<uint64_t>(B) * H;
+    if (!encode_tmap_bf16_3d(&p.tq, q, D, N, BH, 64, BT) || !encode_tmap_bf16_3d(&p.tk, k, D, N, BH, 64, BT) ||
+        !encode_tmap_bf16_3d(&p.tv, v, D, N, BH, 64, BT) || !encode_tmap_bf16_3d(&p.tdo, dout, D, N, BH, 64, BT))
+        return cudaErrorInvalidValue;
+    p.lse = lse;
+    p.dsum = dsum;
+    p.err = device_status_word();
+    if (!p.err) return cudaErrorInvalidDevice;
+    p.N = N;
+    p.BH = static_cast<int>(BH);
+    p.H = H;
+    p.NT = (N + BT - 1) / BT;
+    p.num_items = p.NT * p.BH;
+    p.causal = causal;
+    p.c1 = kLog2e / sqrtf(static_cast<float>(D));
+    p.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(D));
+    p.slopes = slopes;
+    const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
+
+    p.g0 = static_cast<__nv_bfloat16 *>(dk);
+    p.g1 = static_cast<__nv_bfloat16 *>(dv);
+    bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    p.g0 = static_cast<__nv_bfloat16 *>(dq);
+    p.g1 = nullptr;
+    bwd_dq_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int BH, int N) { return static_cast<size_t>(BH) * N * sizeof(float) + 256; }
+
+cudaError_t launch_bwd_tc(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                          const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal,
+                          const Slopes &slopes, cudaStream_t stream)
+{
+    if (d != 128 && d != 64) return cudaErrorInvalidValue;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bwd_workspace_bytes(B * H, N), decode_pool(), stream);
+    if (e != cudaSuccess) return e;
+    float *dsum = static_cast<float *>(ws);
+    e = d == 128 ? launch_bwd_d<128>(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, causal, slopes, dsum, stream)
+                 : launch_bwd_d<64>(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, causal, slopes, dsum, stream);
+    const cudaError_t f = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : f;
+}
+
+}  // namespace alibi

@@ -265,6 +265,44 @@ int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, fl
                                    static_cast<cudaStream_t>(stream)));
 }
 
+int alibi_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse, const void *dout,
+                   void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal, const alibi_fwd_options *opt,
+                   void *stream)
+{
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
+    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (opt && opt->flags != 0u) return ALIBI_ERR_UNSUPPORTED;
+    if (opt && opt->slopes && !slopes_ok(H, opt->slopes)) return ALIBI_ERR_INVALID;
+    Slopes s;
+    if (opt && opt->slopes)
+        fill_slopes_from(H, opt->slopes, &s);
+    else
+        fill_slopes(H, &s);
+    return to_status(launch_bwd_tc(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, d, causal, s,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_bwd_f32(const float *q, const float *k, const float *v, const float *out, const float *lse,
+                       const float *dout, float *dq, float *dk, float *dv, int B, int H, int N, int d, int causal,
+                       void *stream)
+{
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
+    if (d > 256) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_bwd_f32(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, d, causal, s,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const float *slopes,
                          int *first_tile, void *stream)
 {

@@ -64,6 +64,12 @@ cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, f
                              int d, int causal, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
                           const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                          const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal,
+                          const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const float *out, const float *lse,
+                           const float *dout, float *dq, float *dk, float *dv, int B, int H, int N, int d, int causal,
+                           const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(cudaStream_t stream);
 cudaError_t launch_underflow(const void *q, const void *k, int B, int H, int N, int d, float tau,
                              unsigned long long *counts, const Slopes &slopes, cudaStream_t stream);

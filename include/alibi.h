@@ -152,6 +152,35 @@ ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, i
                    int *first_tile, void *stream);
 
 /*
+ * Backward of alibi_attn_fwd / alibi_attn_fwd_ex: the gradients of sum(dout * out)
+ * with respect to q, k and v. There is no trainable parameter in the bias; the
+ * weights are recomputed from the forward's LSE (P_ij = exp(x_ij - lse_i)), so
+ * a weight that underflowed in the forward carries no gradient here either
+ * ("When Attention Goes Blind", sec. 5.1).
+ *   dV = P^T dO,  dS = P o (dO V^T - rowsum(dO o O)),  dQ = dS K / sqrt(d),
+ *   dK = dS^T Q / sqrt(d).
+ * q, k, v, out, dout, dq, dk, dv: device bf16 [B, H, N, d] (out is the
+ * forward's output); lse: device fp32 [B, H, N] (the forward's natural-log
+ * LSE). All device pointers 16-byte aligned. d in {64, 128}; causal as in the
+ * forward; opt: NULL, or an alibi_fwd_options with flags = 0 and optional
+ * slopes (the sec. 3.4 mitigations have no backward yet: ALIBI_ERR_UNSUPPORTED).
+ * Deterministic (no atomics). Takes B*H*N*4 bytes of scratch from the
+ * library's stream-ordered pool for the row sums.
+ */
+ALIBI_API int alibi_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal,
+                   const alibi_fwd_options *opt, void *stream);
+
+/*
+ * alibi_attn_bwd in fp32 at reference precision (CUDA cores, IEEE expf): all
+ * tensors device fp32 with the same layouts; lse from alibi_attn_fwd_f32;
+ * d in [1, 256]; default slopes.
+ */
+ALIBI_API int alibi_attn_bwd_f32(const float *q, const float *k, const float *v, const float *out,
+                   const float *lse, const float *dout, float *dq, float *dk, float *dv, int B, int H, int N,
+                   int d, int causal, void *stream);
+
+/*
  * Causal prefill in fp32 (reference precision): all inputs, outputs and
  * arithmetic in fp32 on the CUDA cores with IEEE expf. Same layouts and
  * semantics as alibi_attn_fwd (causal = 0: symmetric bias); d in [1, 256];

@@ -158,3 +158,17 @@ def test_explicit_slopes_bit_exact_vs_oracle(lib):
             ab.alibi_slopes_explicit(*bad)
     with pytest.raises(ab.AlibiError):
         ab.alibi_slopes_explicit(4, 16, 64, tau=0.0)
+
+
+def test_bwd_argument_errors(lib):
+    f = lib.alibi_attn_bwd
+    assert f(None, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, None, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, P, P, P, MIS, 1, 1, 8, 64, 1, None, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 2, None, None) == ab.ALIBI_ERR_INVALID
+    assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 32, 1, None, None) == ab.ALIBI_ERR_UNSUPPORTED
+    o, keep = _opt(2, -3.0)  # mitigations have no backward
+    assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_UNSUPPORTED
+    o, keep = _opt(0, 0.0, 0.0, [float("nan")])
+    assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_bwd_f32(P, P, P, P, P, P, P, P, P, 1, 1, 8, 300, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_bwd_f32(P, P, P, None, P, P, P, P, P, 1, 1, 8, 16, 1, None) == ab.ALIBI_ERR_INVALID

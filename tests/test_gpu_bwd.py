@@ -1,0 +1,149 @@
+"""Backward pass (dQ, dK, dV of sum(dO * O)) through the C ABI against the fp64
+oracle's gradients, which are pinned to finite differences of the forward.
+
+Tolerances. fp32 path: max-abs error <= 1e-5 x max(1, max |G|) per gradient
+tensor G (the 1e-5 of the forward, scaled to the gradient's magnitude). bf16
+tensor-core path: P and dS enter the tensor-core products rounded to bf16
+(relative 2^-9 each) and the results are rounded to bf16 (half an ulp, allowed
+on top); the largest term is D_i = dO_i . O_i taken from the forward's bf16
+output, whose rounding (2^-9 |dO_i| |O_i|) reaches every dS_ij of the row. When a
+row's weight sits on one key (steep heads) dP_ij - D_i cancels and that error is
+left alone: with N(0, 1) data at d <= 128 it reaches ~2^-6 of the gradient
+scale, so the test allows 2^-5 x max(1, max |G|) per (b, h).
+"""
+import numpy as np
+import pytest
+
+import alibi_inputs as gen
+import oracle
+from gpu_helpers import dev, half_ulp_bf16, host64
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32_REL = 1e-5
+TOL_BF16_REL = 2.0 ** -5
+
+
+@pytest.fixture(scope="module")
+def ab():
+    import alibi_positional_bias_gb300 as ab
+    ab.load()
+    return ab
+
+
+def check_grad(got, ref, rel, what, bf16=False):
+    B, H = ref.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            g, r = got[b, h], ref[b, h]
+            scale = max(1.0, float(np.abs(r).max()))
+            lim = rel * scale + (half_ulp_bf16(r) if bf16 else 0.0)
+            err = np.abs(g - r)
+            assert np.isfinite(g).all(), f"{what}[{b},{h}]: non-finite"
+            assert (err <= lim).all(), (f"{what}[{b},{h}]: max err {err.max():.3e}, scale {scale:.3e}, "
+                                        f"worst excess {(err - lim).max():.3e}")
+
+
+def cases(seed, B, H, N, d, dtype):
+    q, k, v = gen.random_case(seed, B, H, N, d, dtype=dtype)
+    do, _, _ = gen.random_case(seed + 1000, B, H, N, d, dtype=dtype)
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("B,H,N,d", [(1, 4, 64, 16), (2, 3, 100, 64), (1, 2, 77, 200), (1, 1, 1, 32)])
+def test_bwd_f32_vs_oracle(ab, B, H, N, d, causal):
+    q, k, v, do = cases(11 + N + d, B, H, N, d, "fp32")
+    qd, kd, vd, dod = (dev(t, "fp32") for t in (q, k, v, do))
+    out, lse = ab.alibi_attn_fwd_f32(qd, kd, vd, causal=causal)
+    dq, dk, dv = ab.alibi_attn_bwd_f32(qd, kd, vd, out, lse, dod, causal=causal)
+    ab.alibi_check_error()
+    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal)
+    check_grad(host64(dq), rq, TOL_F32_REL, "dq")
+    check_grad(host64(dk), rk, TOL_F32_REL, "dk")
+    check_grad(host64(dv), rv, TOL_F32_REL, "dv")
+
+
+def run_bf16(ab, q, k, v, do, causal=True, slopes=None):
+    qd, kd, vd, dod = (dev(t, "bf16") for t in (q, k, v, do))
+    if slopes is None:
+        out, lse = ab.alibi_attn_fwd(qd, kd, vd, causal=causal)
+    else:
+        out, lse = ab.alibi_attn_fwd_ex(qd, kd, vd, causal=causal, slopes=slopes)
+    dq, dk, dv = ab.alibi_attn_bwd(qd, kd, vd, out, lse, dod, causal=causal, slopes=slopes)
+    ab.alibi_check_error()
+    return host64(dq), host64(dk), host64(dv)
+
+
+# single tile, ragged tiles, several tiles (both kernels' walks), both head sizes
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 1, 64), (1, 2, 7, 128), (1, 2, 128, 64), (1, 3, 129, 128),
+                                     (2, 2, 300, 64), (1, 4, 513, 128), (1, 2, 1000, 128)])
+def test_bwd_bf16_vs_oracle(ab, B, H, N, d, causal):
+    q, k, v, do = cases(21 + N + d, B, H, N, d, "bf16")
+    dq, dk, dv = run_bf16(ab, q, k, v, do, causal)
+    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal)
+    check_grad(dq, rq, TOL_BF16_REL, "dq", bf16=True)
+    check_grad(dk, rk, TOL_BF16_REL, "dk", bf16=True)
+    check_grad(dv, rv, TOL_BF16_REL, "dv", bf16=True)
+
+
+def test_bwd_bf16_explicit_slopes(ab):
+    H, N, d = 9, 600, 64
+    m = ab.alibi_slopes_explicit(H, 16, 4096)
+    q, k, v, do = cases(31, 1, H, N, d, "bf16")
+    dq, dk, dv = run_bf16(ab, q, k, v, do, slopes=m)
+    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, m=m.astype(np.float64))
+    check_grad(dq, rq, TOL_BF16_REL, "dq", bf16=True)
+    check_grad(dk, rk, TOL_BF16_REL, "dk", bf16=True)
+    check_grad(dv, rv, TOL_BF16_REL, "dv", bf16=True)
+
+
+def test_bwd_identities_at_layer_size(ab):
+    # layer_n2048 shapes (B=4, H=32, N=2048, d=128): rows of P sum to one and rows of dS
+    # to zero, so per (b, h): sum_j dV_j = sum_i dO_i and sum_j dK_j = 0.
+    w = gen.WORKLOADS["layer_n2048"]
+    q, k, v = gen.generate(w)
+    do, _, _ = gen.random_case(77, w.B, w.H, w.N, w.d, dtype="bf16")
+    dq, dk, dv = run_bf16(ab, q, k, v, do)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+    sum_do = do.f32.astype(np.float64).sum(axis=2)
+    assert np.abs(dv.sum(axis=2) - sum_do).max() <= 0.05 * max(1.0, np.abs(sum_do).max())
+    assert np.abs(dk.sum(axis=2)).max() <= 0.05 * max(1.0, np.abs(dk).sum(axis=2).max())
+    # one full head against the oracle
+    h = 5
+    sl = (slice(0, 1), slice(h, h + 1))
+    m = oracle.slopes(w.H)[h:h + 1]
+    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], m=m)
+    check_grad(dq[sl], rq, TOL_BF16_REL, "dq", bf16=True)
+    check_grad(dk[sl], rk, TOL_BF16_REL, "dk", bf16=True)
+    check_grad(dv[sl], rv, TOL_BF16_REL, "dv", bf16=True)
+
+
+def test_bwd_deterministic(ab):
+    import torch
+    q, k, v, do = cases(41, 1, 4, 700, 128, "bf16")
+    qd, kd, vd, dod = (dev(t, "bf16") for t in (q, k, v, do))
+    out, lse = ab.alibi_attn_fwd(qd, kd, vd)
+    g1 = ab.alibi_attn_bwd(qd, kd, vd, out, lse, dod)
+    g2 = ab.alibi_attn_bwd(qd, kd, vd, out, lse, dod)
+    ab.alibi_check_error()
+    assert all(torch.equal(a, b) for a, b in zip(g1, g2))
+
+
+def test_bwd_far_keys_get_exactly_zero_gradient(ab):
+    # "When Attention Goes Blind" sec. 5.1: a weight that underflowed carries no
+    # gradient. Slope 1 (blindness distance 88), dO nonzero only for rows 150 and
+    # beyond: in fp64 key 0 still gets a tiny dV (below e^-140), on the GPU exactly 0.
+    H, N, d = 2, 256, 64
+    q, k, v, do = cases(51, 1, H, N, d, "bf16")
+    dob = do.f32.copy()
+    dob[:, :, :150] = 0.0
+    do = gen.make_tensor(dob, dob.shape, "bf16")
+    m = np.ones(H, np.float32)
+    dq, dk, dv = run_bf16(ab, q, k, v, do, slopes=m)
+    _, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, m=m.astype(np.float64))
+    assert (np.abs(rv[0, :, 0]) > 0).any() and np.abs(rv[0, :, 0]).max() < 1e-55
+    assert not dv[0, :, 0].any() and not dk[0, :, 0].any()
+    # keys within reach of the nonzero rows do get gradient
+    assert np.abs(dv[0, :, 200]).max() > 0
