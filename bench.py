@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--no-underflow", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     # profiling helpers: run one kernel family on a reduced instance of its workload
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None)
+    ap.add_argument("--only", choices=["prefill", "decode", "backward"], default=None)
     ap.add_argument("--prefill-heads", type=int, default=None, help="override H of the prefill workload")
     ap.add_argument("--decode-batch", type=int, default=None, help="override B of the decode workload")
     return ap.parse_args()
@@ -243,7 +243,7 @@ def run_native(args):
         wp = gen.Workload(**{**wp.__dict__, "H": args.prefill_heads})
     if args.decode_batch:
         wd = gen.Workload(**{**wd.__dict__, "B": args.decode_batch})
-    do_pre = args.only in (None, "prefill")
+    do_pre = args.only in (None, "prefill", "backward")
     do_dec = args.only in (None, "decode")
 
     # Inputs resident in HBM before the timed region. With N ranks the job is a
@@ -275,6 +275,29 @@ def run_native(args):
     splits = ab.alibi_attn_decode_splits(wd.B, wd.H, wd.N, wd.d)
     launches_per_step = int(do_pre) + (2 if splits > 1 else 1) * int(do_dec)
     stream = torch.cuda.current_stream(dev)
+
+    if args.only == "backward":  # profiling run: the backward kernels alone
+        wdo = gen.Workload(**{**wpg.__dict__, "seed": wpg.seed + 1})
+        do_b = torch.empty_like(q)
+        gen.fill_device(wdo, 0, do_b, start=shard_batch(wpg.B, world, rank)[0] * wp.H * wp.N * wp.d)
+        ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream)
+        grads = [torch.empty_like(q) for _ in range(3)]
+        for _ in range(args.warmup):
+            ab.alibi_attn_bwd(q, k, v, out, lse, do_b, *grads, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            ab.alibi_attn_bwd(q, k, v, out, lse, do_b, *grads, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ab.alibi_check_error(stream)
+        ms = e0.elapsed_time(e1) / args.steps
+        if rank == 0:
+            print(json.dumps({"profile_run": "backward", "backward_ms": ms,
+                              "algorithmic_tflops": 2.5 * prefill_flops(wp) / (ms / 1e3) / 1e12}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     def step(evs=None):
         flush.fill_(1.0)  # L2 flush, outside the event-timed launches
@@ -357,7 +380,7 @@ def run_native(args):
 
     tile_flops = 4.0 * 128 * 128 * wp.d  # QK^T + PV of one 128 x 128 tile
     # -------------------- exact underflow-tile skipping, same inputs, own timing
-    skip = noncausal = steep = None
+    skip = noncausal = steep = backward = None
     if do_pre:
         tiles_run, tiles_all = tiles_kept(ab.alibi_attn_skip_plan(q, k).cpu().numpy())
         t_skip = timed_ms(lambda: ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True))
@@ -384,6 +407,23 @@ def run_native(args):
                  "tiles_skipped_frac": 1.0 - run_s / all_s,
                  "algorithmic_tflops_skip": world * prefill_flops(wp) / (t_ss / 1e3) / 1e12,
                  "executed_tflops_skip": world * run_s * tile_flops / (t_ss / 1e3) / 1e12}
+
+        # -------------------- backward of the same layer (dQ, dK, dV from out, lse and dO ~ N(0, 1)):
+        # 5 B H N^2 d flops at the causal count (2.5x the forward); the two kernels execute 7
+        # (S and dP are computed in both). Inputs: the forward's own out and lse.
+        wdo = gen.Workload(**{**wpg.__dict__, "seed": wpg.seed + 1})
+        do_b = torch.empty_like(q)
+        gen.fill_device(wdo, 0, do_b, start=shard_batch(wpg.B, world, rank)[0] * wp.H * wp.N * wp.d)
+        ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        t_bwd = timed_ms(lambda: ab.alibi_attn_bwd(q, k, v, out, lse, do_b, gq, gk, gv, stream=stream))
+        bwd_tf = 2.5 * prefill_flops(wp) / (t_bwd / 1e3) / 1e12
+        backward = {"ms": t_bwd, "algorithmic_tflops": world * bwd_tf, "unit": "TFLOP/s",
+                    "frac": bwd_tf / peaks["bf16_tflops"],
+                    "executed_tflops": world * 3.5 * prefill_flops(wp) / (t_bwd / 1e3) / 1e12,
+                    "launches": 3,  # D = rowsum(dO o O), dK/dV kernel, dQ kernel
+                    "peak_source": f"bf16 dense burst, {peaks['source']}"}
+        del do_b, gq, gk, gv
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
@@ -503,6 +543,7 @@ def run_native(args):
         "prefill_skip_underflow": skip,
         "prefill_noncausal": noncausal,
         "prefill_steep_slopes": steep,
+        "backward": backward,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
