@@ -226,9 +226,10 @@ def alibi_slopes_explicit(H: int, delta_first: float, delta_last: float, tau: fl
 
 
 def alibi_attn_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, causal: bool = True, slopes=None,
-                   stream=None):
+                   flags: int = 0, clamp_min: float = -87.0, softcap_z: float = 50.0, stream=None):
     """bf16 backward on the tensor cores: (dq, dk, dv) of sum(dout * out) for the
-    forward's out and lse. All tensors [B, H, N, d] bf16 CUDA tensors, lse fp32."""
+    forward's out and lse. All tensors [B, H, N, d] bf16 CUDA tensors, lse fp32.
+    flags / clamp_min / softcap_z / slopes must be those the forward ran with."""
     import torch
     _need(q, torch.bfloat16, None, "q")
     B, H, N, d = q.shape
@@ -245,7 +246,8 @@ def alibi_attn_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, causal: b
         m = np.ascontiguousarray(slopes, dtype=np.float32)
         if m.shape != (H,):
             raise ValueError(f"slopes: expected shape ({H},), got {m.shape}")
-    opt = AlibiFwdOptions(0, 0.0, 0.0, None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    opt = AlibiFwdOptions(int(flags), float(clamp_min), float(softcap_z),
+                          None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     _check(load().alibi_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, H, N, d, int(bool(causal)), ctypes.byref(opt),
                                  _stream(stream, q.device)), "alibi_attn_bwd")

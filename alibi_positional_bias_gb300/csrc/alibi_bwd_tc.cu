@@ -11,7 +11,10 @@
 //   P_ij  = exp(x_ij - LSE_i),   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,
 //   dS_ij = P_ij (dP_ij - D_i),
 //   dV = P^T dO,   dK = dS^T Q / sqrt(d),   dQ = dS K / sqrt(d).
-// The bias has no trainable parameter and enters only through P.
+// The bias has no trainable parameter and enters only through P. With the
+// mitigations of sec. 3.4 (the VAR instantiations) P is recomputed with the
+// clamped / log-distance bias and the soft-capped logit, and the soft cap's
+// derivative 1 - tanh^2(A / z) multiplies dS before it meets K or Q.
 //
 // Three launches, no atomics (the result is deterministic):
 //   bwd_prep_kernel   D_i = dO_i . O_i (fp32 from the bf16 tensors)
@@ -69,8 +72,45 @@ struct BwdParams {
     int N, BH, H, NT, num_items, causal;
     float c1;       // log2(e) / sqrt(d)
     float inv_sqrt_d;
+    // mitigations (kFwdClamp / kFwdLogDist / kFwdSoftcap), constants in base-2 units as in the forward
+    unsigned int variant;
+    float clamp2, cap_k, cap_zl;
     Slopes slopes;
 };
+
+__device__ __forceinline__ float lg2_approx_b(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx_b(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One element with the mitigations, base-2 units: raw score sv, distance |i - j|
+// (exact integer in fp32), the row / column's -LSE log2(e). Returns P and sets
+// *fac to d(capped logit)/d(raw logit).
+__device__ __forceinline__ float var_weight(const BwdParams &p, float mnat, float sl2, float sv, float dist,
+                                            float nlse2, float *fac)
+{
+    const bool cap = p.variant & kFwdSoftcap, logd = p.variant & kFwdLogDist, clamp = p.variant & kFwdClamp;
+    float a = sv * p.c1, f = 1.0f;
+    if (cap) {
+        // z tanh(A / z) with tanh(y) = 1 - 2 / (e^{2y} + 1); the derivative is 1 - tanh^2
+        const float th = fmaf(-2.0f, rcp_approx_b(ex2_approx(sv * p.cap_k) + 1.0f), 1.0f);
+        a = th * p.cap_zl;
+        f = (1.0f - th) * (1.0f + th);
+    }
+    float b = logd ? -mnat * lg2_approx_b(dist + 1.0f) : -sl2 * dist;
+    if (clamp) b = fmaxf(b, p.clamp2);
+    *fac = f;
+    return ex2_approx(a + b + nlse2);
+}
 
 enum : uint32_t {
     SITE_B_PROD_RES = 0x401, SITE_B_PROD_RING = 0x402, SITE_B_MMA_RES = 0x411, SITE_B_MMA_RING = 0x412,
@@ -163,7 +203,7 @@ __device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0
 
 // ------------------------------------------------------------------ dK, dV
 
-template <int D>
+template <int D, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p)
 {
     using C = BwdCfg<D>;
@@ -352,21 +392,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 const float base = sl2 * static_cast<float>((qt - t.tile) * BT + 64 * s - r);
                 const bool diag = p.causal && qt == t.tile;
                 uint32_t pk[32], dk[32];
+                if (VAR) {
+                    const float mnat = p.slopes.nat[t.bh % p.H];
+                    const float di = static_cast<float>((qt - t.tile) * BT + 64 * s - r);  // i - j at c = 0
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    float pv[2], dv[2];
+                    for (int u = 0; u < 32; ++u) {
+                        float pv[2], dv[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int c = 2 * u + e;
-                        const float tt = fmaf(sl2, static_cast<float>(c), base);
-                        const float b = p.causal ? -tt : -fabsf(tt);
-                        float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) - buf[c];
-                        if (diag && 64 * s + c < r) x = -INFINITY;  // query before key: masked
-                        pv[e] = ex2_approx(x);
-                        dv[e] = pv[e] * (__uint_as_float(draw[c]) - buf[64 + c]);
+                        for (int e = 0; e < 2; ++e) {
+                            const int c = 2 * u + e;
+                            float f;
+                            float w = var_weight(p, mnat, sl2, __uint_as_float(sraw[c]),
+                                                 fabsf(di + static_cast<float>(c)), -buf[c], &f);
+                            if (diag && 64 * s + c < r) w = 0.f;  // query before key: masked
+                            pv[e] = w;
+                            dv[e] = w * (__uint_as_float(draw[c]) - buf[64 + c]) * f;
+                        }
+                        pk[u] = pack_bf16x2(pv[0], pv[1]);
+                        dk[u] = pack_bf16x2(dv[0], dv[1]);
                     }
-                    pk[u] = pack_bf16x2(pv[0], pv[1]);
-                    dk[u] = pack_bf16x2(dv[0], dv[1]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        float pv[2], dv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int c = 2 * u + e;
+                            const float tt = fmaf(sl2, static_cast<float>(c), base);
+                            const float b = p.causal ? -tt : -fabsf(tt);
+                            float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) - buf[c];
+                            if (diag && 64 * s + c < r) x = -INFINITY;  // query before key: masked
+                            pv[e] = ex2_approx(x);
+                            dv[e] = pv[e] * (__uint_as_float(draw[c]) - buf[64 + c]);
+                        }
+                        pk[u] = pack_bf16x2(pv[0], pv[1]);
+                        dk[u] = pack_bf16x2(dv[0], dv[1]);
+                    }
                 }
                 tmem_st32(lane_addr + kColS + 64 * s, pk);
                 tmem_st32(lane_addr + kColP + 64 * s, dk);
@@ -402,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 
 // ---------------------------------------------------------------------- dQ
 
-template <int D>
+template <int D, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
     using C = BwdCfg<D>;
@@ -563,20 +624,39 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 const bool diag = p.causal && it == t.tile;
                 const float nl = -lse2;
                 uint32_t dk[32];
+                if (VAR) {
+                    const float mnat = p.slopes.nat[t.bh % p.H];
+                    const float di = static_cast<float>(i - it * BT - 64 * s);  // i - k at c = 0
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    float dv[2];
+                    for (int u = 0; u < 32; ++u) {
+                        float dv[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int c = 2 * u + e;
-                        const float tt = fmaf(sl2, static_cast<float>(c), nb);
-                        const float b = p.causal ? tt : -fabsf(tt);
-                        float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) + nl;
-                        if (diag && 64 * s + c > r) x = -INFINITY;  // key after the query: masked
-                        const float pv = ex2_approx(x);
-                        dv[e] = pv * (__uint_as_float(draw[c]) - Di);
+                        for (int e = 0; e < 2; ++e) {
+                            const int c = 2 * u + e;
+                            float f;
+                            float w = var_weight(p, mnat, sl2, __uint_as_float(sraw[c]),
+                                                 fabsf(di - static_cast<float>(c)), nl, &f);
+                            if (diag && 64 * s + c > r) w = 0.f;  // key after the query: masked
+                            dv[e] = w * (__uint_as_float(draw[c]) - Di) * f;
+                        }
+                        dk[u] = pack_bf16x2(dv[0], dv[1]);
                     }
-                    dk[u] = pack_bf16x2(dv[0], dv[1]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        float dv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int c = 2 * u + e;
+                            const float tt = fmaf(sl2, static_cast<float>(c), nb);
+                            const float b = p.causal ? tt : -fabsf(tt);
+                            float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) + nl;
+                            if (diag && 64 * s + c > r) x = -INFINITY;  // key after the query: masked
+                            const float pv = ex2_approx(x);
+                            dv[e] = pv * (__uint_as_float(draw[c]) - Di);
+                        }
+                        dk[u] = pack_bf16x2(dv[0], dv[1]);
+                    }
                 }
                 tmem_st32(lane_addr + kColS + 64 * s, dk);
                 tmem_wait_st();
@@ -644,16 +724,17 @@ cudaError_t check_launch_regs(K kernel, uint32_t smem)
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int D>
+template <int D, bool VAR>
 cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void *out, const float *lse,
                          const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int causal,
-                         const Slopes &slopes, float *dsum, cudaStream_t stream)
+                         unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes, float *dsum,
+                         cudaStream_t stream)
 {
     using C = BwdCfg<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = check_launch_regs(bwd_dkdv_kernel<D>, C::kSmem);
-        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D>, C::kSmem);
+        cudaError_t e = check_launch_regs(bwd_dkdv_kernel<D, VAR>, C::kSmem);
+        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D, VAR>, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -682,15 +763,19 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     p.c1 = kLog2e / sqrtf(static_cast<float>(D));
     p.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(D));
     p.slopes = slopes;
+    p.variant = flags & (kFwdClamp | kFwdLogDist | kFwdSoftcap);
+    p.clamp2 = clamp_min * kLog2e;
+    p.cap_k = (flags & kFwdSoftcap) ? 2.0f * kLog2e / (sqrtf(static_cast<float>(D)) * softcap_z) : 0.f;
+    p.cap_zl = softcap_z * kLog2e;
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
 
     p.g0 = static_cast<__nv_bfloat16 *>(dk);
     p.g1 = static_cast<__nv_bfloat16 *>(dv);
-    bwd_dkdv_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(p);
+    bwd_dkdv_kernel<D, VAR><<<grid, kThreads, C::kSmem, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
-    bwd_dq_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(p);
+    bwd_dq_kernel<D, VAR><<<grid, kThreads, C::kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -700,15 +785,21 @@ size_t bwd_workspace_bytes(int BH, int N) { return static_cast<size_t>(BH) * N *
 
 cudaError_t launch_bwd_tc(const void *q, const void *k, const void *v, const void *out, const float *lse,
                           const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal,
-                          const Slopes &slopes, cudaStream_t stream)
+                          unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
+                          cudaStream_t stream)
 {
     if (d != 128 && d != 64) return cudaErrorInvalidValue;
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, bwd_workspace_bytes(B * H, N), decode_pool(), stream);
     if (e != cudaSuccess) return e;
     float *dsum = static_cast<float *>(ws);
-    e = d == 128 ? launch_bwd_d<128>(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, causal, slopes, dsum, stream)
-                 : launch_bwd_d<64>(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, causal, slopes, dsum, stream);
+    const bool var = (flags & (kFwdClamp | kFwdLogDist | kFwdSoftcap)) != 0;
+#define ALIBI_BWD_ARGS q, k, v, out, lse, dout, dq, dk, dv, B, H, N, causal, flags, clamp_min, softcap_z, slopes, dsum, stream
+    if (d == 128)
+        e = var ? launch_bwd_d<128, true>(ALIBI_BWD_ARGS) : launch_bwd_d<128, false>(ALIBI_BWD_ARGS);
+    else
+        e = var ? launch_bwd_d<64, true>(ALIBI_BWD_ARGS) : launch_bwd_d<64, false>(ALIBI_BWD_ARGS);
+#undef ALIBI_BWD_ARGS
     const cudaError_t f = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : f;
 }

@@ -277,15 +277,22 @@ int alibi_attn_bwd(const void *q, const void *k, const void *v, const void *out,
     if (st != ALIBI_OK) return st;
     if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
     if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
-    if (opt && opt->flags != 0u) return ALIBI_ERR_UNSUPPORTED;
-    if (opt && opt->slopes && !slopes_ok(H, opt->slopes)) return ALIBI_ERR_INVALID;
+    const alibi_fwd_options none = {0u, 0.0f, 0.0f, nullptr};
+    if (!opt) opt = &none;
+    const unsigned int mit = ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP;
+    if (opt->flags & ~(mit | ALIBI_FWD_SKIP_UNDERFLOW)) return ALIBI_ERR_INVALID;
+    if (opt->flags & ALIBI_FWD_SKIP_UNDERFLOW) return ALIBI_ERR_UNSUPPORTED;
+    if ((opt->flags & ALIBI_FWD_CLAMP) && !(opt->clamp_min < 0.0f)) return ALIBI_ERR_INVALID;
+    if ((opt->flags & ALIBI_FWD_SOFTCAP) && !(opt->softcap_z > 0.0f && std::isfinite(opt->softcap_z)))
+        return ALIBI_ERR_INVALID;
+    if (opt->slopes && !slopes_ok(H, opt->slopes)) return ALIBI_ERR_INVALID;
     Slopes s;
-    if (opt && opt->slopes)
+    if (opt->slopes)
         fill_slopes_from(H, opt->slopes, &s);
     else
         fill_slopes(H, &s);
-    return to_status(launch_bwd_tc(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, d, causal, s,
-                                   static_cast<cudaStream_t>(stream)));
+    return to_status(launch_bwd_tc(q, k, v, out, lse, dout, dq, dk, dv, B, H, N, d, causal, opt->flags,
+                                   opt->clamp_min, opt->softcap_z, s, static_cast<cudaStream_t>(stream)));
 }
 
 int alibi_attn_bwd_f32(const float *q, const float *k, const float *v, const float *out, const float *lse,

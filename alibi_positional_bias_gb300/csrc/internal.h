@@ -66,7 +66,8 @@ cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *o
                           const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_bwd_tc(const void *q, const void *k, const void *v, const void *out, const float *lse,
                           const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal,
-                          const Slopes &slopes, cudaStream_t stream);
+                          unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
+                          cudaStream_t stream);
 cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const float *out, const float *lse,
                            const float *dout, float *dq, float *dk, float *dv, int B, int H, int N, int d, int causal,
                            const Slopes &slopes, cudaStream_t stream);

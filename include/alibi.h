@@ -161,9 +161,11 @@ ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, i
  *   dK = dS^T Q / sqrt(d).
  * q, k, v, out, dout, dq, dk, dv: device bf16 [B, H, N, d] (out is the
  * forward's output); lse: device fp32 [B, H, N] (the forward's natural-log
- * LSE). All device pointers 16-byte aligned. d in {64, 128}; causal as in the
- * forward; opt: NULL, or an alibi_fwd_options with flags = 0 and optional
- * slopes (the sec. 3.4 mitigations have no backward yet: ALIBI_ERR_UNSUPPORTED).
+ * LSE). All device pointers 16-byte aligned. d in {64, 128}; causal and opt
+ * exactly as the forward ran (NULL: defaults). With ALIBI_FWD_CLAMP / _LOGDIST
+ * the weights are recomputed with that bias; with ALIBI_FWD_SOFTCAP dS is also
+ * multiplied by the cap's derivative 1 - tanh^2(A / z) before it meets K or Q.
+ * ALIBI_FWD_SKIP_UNDERFLOW has no backward (ALIBI_ERR_UNSUPPORTED).
  * Deterministic (no atomics). Takes B*H*N*4 bytes of scratch from the
  * library's stream-ordered pool for the row sums.
  */

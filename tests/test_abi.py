@@ -166,8 +166,12 @@ def test_bwd_argument_errors(lib):
     assert f(P, P, P, P, P, P, P, P, MIS, 1, 1, 8, 64, 1, None, None) == ab.ALIBI_ERR_INVALID
     assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 2, None, None) == ab.ALIBI_ERR_INVALID
     assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 32, 1, None, None) == ab.ALIBI_ERR_UNSUPPORTED
-    o, keep = _opt(2, -3.0)  # mitigations have no backward
+    o, keep = _opt(1)  # skipping has no backward
     assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_UNSUPPORTED
+    o, keep = _opt(2, 1.0)  # clamp >= 0
+    assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_INVALID
+    o, keep = _opt(32)  # unknown flag
+    assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_INVALID
     o, keep = _opt(0, 0.0, 0.0, [float("nan")])
     assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_bwd_f32(P, P, P, P, P, P, P, P, P, 1, 1, 8, 300, 1, None) == ab.ALIBI_ERR_UNSUPPORTED

@@ -147,3 +147,34 @@ def test_bwd_far_keys_get_exactly_zero_gradient(ab):
     assert not dv[0, :, 0].any() and not dk[0, :, 0].any()
     # keys within reach of the nonzero rows do get gradient
     assert np.abs(dv[0, :, 200]).max() > 0
+
+
+ABI = {"clamp": 2, "logdist": 4, "softcap": 8}
+ORC = {"clamp": oracle.CLAMP, "logdist": oracle.LOGDIST, "softcap": oracle.SOFTCAP}
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("combo", [("clamp",), ("logdist",), ("softcap",), ("clamp", "logdist", "softcap")],
+                         ids=["clamp", "logdist", "softcap", "all3"])
+def test_bwd_mitigations(ab, combo, causal):
+    # sigma = 3 on Q and K with z = 8 puts many logits on the curved part of the cap
+    # (its derivative factor matters); c_clamp = -3 makes the clamp bind.
+    B, H, N, d = 1, 3, 300, 128
+    q, k, _ = gen.random_case(61, B, H, N, d, dtype="bf16", sigma=3.0)
+    _, _, v = gen.random_case(62, B, H, N, d, dtype="bf16")
+    do, _, _ = gen.random_case(63, B, H, N, d, dtype="bf16")
+    flags = sum(ABI[c] for c in combo)
+    kw = dict(flags=flags, clamp_min=-3.0, softcap_z=8.0)
+    qd, kd, vd, dod = (dev(t, "bf16") for t in (q, k, v, do))
+    out, lse = ab.alibi_attn_fwd_ex(qd, kd, vd, causal=causal, **kw)
+    dq, dk, dv = ab.alibi_attn_bwd(qd, kd, vd, out, lse, dod, causal=causal, **kw)
+    ab.alibi_check_error()
+    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal,
+                                            variant=sum(ORC[c] for c in combo), c_clamp=-3.0, z_cap=8.0)
+    check_grad(host64(dq), rq, TOL_BF16_REL, "dq", bf16=True)
+    check_grad(host64(dk), rk, TOL_BF16_REL, "dk", bf16=True)
+    check_grad(host64(dv), rv, TOL_BF16_REL, "dv", bf16=True)
+    if "softcap" in combo:
+        # the cap's derivative is not vacuous on these inputs: 1 - tanh^2(A / z) is far from 1
+        a = q.f32[0, 0].astype(np.float64) @ k.f32[0, 0].astype(np.float64).T / np.sqrt(d)
+        assert np.mean(1.0 - np.tanh(a / 8.0) ** 2) < 0.8
