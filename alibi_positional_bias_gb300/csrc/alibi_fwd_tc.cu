@@ -275,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (converged, warp-uniform values); one elected
+        // lane issues each tcgen05 instruction.
+        {
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);
             const uint32_t sQ = smem_u32(smem + C::kQ);
@@ -290,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const Item t = decode_item(p, w);
                 const int last_slot = t.q1valid ? 1 : 0;
                 ok = mbar_wait(&q_full[0], k & 1, err, SITE_MMA_Q) && mbar_wait(&q_full[1], k & 1, err, SITE_MMA_Q);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
 
                 // S_s = Q_s K^T over d in steps of 16 (K-major operands, 32-byte steps inside a
@@ -303,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t step = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-                        mma_ss(dst, qd + step, kd + step, idS, kk > 0);
+                        mma_ss_w(dst, qd + step, kd + step, idS, kk > 0);
                     }
-                    mma_commit(&s_full[s]);
+                    mma_commit_w(&s_full[s]);
                 };
                 // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous;
                 // 16 keys = 2048 bytes per step)
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                     for (int k4 = 0; k4 < BN / 32; ++k4) {
                         const int kk = half * (BN / 32) + k4;
-                        mma_ts(dst, pa + kk * 8, vd + ((kk * 2048) >> 4), idO, (first && kk == 0) ? 0u : 1u);
+                        mma_ts_w(dst, pa + kk * 8, vd + ((kk * 2048) >> 4), idO, (first && kk == 0) ? 0u : 1u);
                     }
                 };
 
@@ -325,54 +328,59 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 {
                     const uint32_t st = kc % 2, ph = (kc / 2) & 1;
                     ok = mbar_wait(&k_full[st], ph, err, SITE_MMA_K);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     for (int s = 0; s < 2; ++s)
                         if (slot_active(p, t, s, 0)) issue_S(s, st);
-                    mma_commit(&k_empty[st]);
+                    mma_commit_w(&k_empty[st]);
                 }
                 for (int it = 0; it < t.n && ok; ++it) {
                     const uint32_t vst = (vc + it) % 2, vph = ((vc + it) / 2) & 1;
                     ok = mbar_wait(&v_full[vst], vph, err, SITE_MMA_V);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     // the next K tile is normally resident long before it is needed: wait
                     // for it here, off the P -> PV -> S critical path
                     if (it + 1 < t.n) {
                         const uint32_t kst = (kc + it + 1) % 2, kph = ((kc + it + 1) / 2) & 1;
                         ok = mbar_wait(&k_full[kst], kph, err, SITE_MMA_K);
+                        ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                     }
                     for (int s = 0; s < 2 && ok; ++s) {
                         if (slot_active(p, t, s, it)) {
                             ok = mbar_wait(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
                             if (ok && first_pv[s]) ok = mbar_wait(&o_empty[s], (o_cnt[s] & 1) ^ 1, err, SITE_MMA_O);
+                            ok = __all_sync(0xffffffffu, ok);
                             if (!ok) break;
                             tc_fence_after();
                             issue_PV_half(s, vst, first_pv[s], 0);
                             ok = mbar_wait(&p_hi[s], p_cnt[s] & 1, err, SITE_MMA_P);
                             ++p_cnt[s];
+                            ok = __all_sync(0xffffffffu, ok);
                             if (!ok) break;
                             tc_fence_after();
                             issue_PV_half(s, vst, first_pv[s], 1);
                             first_pv[s] = false;
                             if (it == t.n - 1) {
-                                mma_commit(&o_full[s]);
+                                mma_commit_w(&o_full[s]);
                                 ++o_cnt[s];
                             }
                         }
                         if (it + 1 < t.n && slot_active(p, t, s, it + 1)) {
                             const uint32_t kst = (kc + it + 1) % 2;
                             issue_S(s, kst);
-                            if (s == last_slot) mma_commit(&k_empty[kst]);
+                            if (s == last_slot) mma_commit_w(&k_empty[kst]);
                         }
                     }
-                    mma_commit(&v_empty[vst]);
+                    mma_commit_w(&v_empty[vst]);
                 }
-                mma_commit(q_empty);
+                mma_commit_w(q_empty);
                 kc += t.n;
                 vc += t.n;
             }
             // drain: every MMA issued above completes before TMEM is released
-            mma_commit(mma_done);
+            mma_commit_w(mma_done);
             mbar_wait(mma_done, 0, err, SITE_MMA_DONE);
         }
     }
