@@ -282,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                     }
                 }
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
+            // whole warp, converged; one elected lane issues each tcgen05 instruction
             // -------------------------------------------------------- MMA issuer
             constexpr uint32_t idS = idesc_bf16_f32(BT, BT, 0);
             constexpr uint32_t idG = idesc_bf16_f32(BT, D, 1);
@@ -296,10 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 if (w >= p.num_items) break;
                 const BItem t = dkdv_item(p, w);
                 ok = mbar_wait(kv_full, k & 1, err, SITE_B_MMA_RES);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 for (int it = 0; it < t.n && ok; ++it, ++qc) {
                     const uint32_t st = qc & 1, ph = (qc >> 1) & 1;
                     ok = mbar_wait(&qo_full[st], ph, err, SITE_B_MMA_RING);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
                     // S^T = K Q^T and dP^T = V dO^T (both operands K-major along d)
@@ -307,15 +310,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                     const uint64_t od = smem_desc_sw128(sO + st * C::kTileBytes, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kColS, kd + kmajor_step<D>(kk), qd + kmajor_step<D>(kk), idS, kk > 0);
+                        mma_ss_w(tmem + kColS, kd + kmajor_step<D>(kk), qd + kmajor_step<D>(kk), idS, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kColP, vd + kmajor_step<D>(kk), od + kmajor_step<D>(kk), idS, kk > 0);
-                    mma_commit(s_full);
+                        mma_ss_w(tmem + kColP, vd + kmajor_step<D>(kk), od + kmajor_step<D>(kk), idS, kk > 0);
+                    mma_commit_w(s_full);
                     // P^T and dS^T written back by the elementwise warps
                     ok = mbar_wait(p_full, pc & 1, err, SITE_B_MMA_P);
                     ++pc;
                     if (ok && it == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
                     // dV += P^T dO, dK += dS^T Q (B operands MN-major: the contraction runs over queries)
@@ -323,19 +327,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                     const uint64_t qmn = smem_desc_sw128(sQ + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), omn + mnmajor_step(kk), idG,
+                        mma_ts_w(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), omn + mnmajor_step(kk), idG,
                                (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts(tmem + kColAcc1, tmem + tmem_a_col(kColP, kk), qmn + mnmajor_step(kk), idG,
+                        mma_ts_w(tmem + kColAcc1, tmem + tmem_a_col(kColP, kk), qmn + mnmajor_step(kk), idG,
                                (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&qo_empty[st]);
+                    mma_commit_w(&qo_empty[st]);
                 }
                 if (!ok) break;
-                mma_commit(kv_empty);
-                mma_commit(acc_full);
+                mma_commit_w(kv_empty);
+                mma_commit_w(acc_full);
             }
-            mma_commit(mma_done);
+            mma_commit_w(mma_done);
             mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE);
         }
     } else {
@@ -540,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                     }
                 }
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
+            // whole warp, converged; one elected lane issues each tcgen05 instruction
             constexpr uint32_t idS = idesc_bf16_f32(BT, BT, 0);
             constexpr uint32_t idG = idesc_bf16_f32(BT, D, 1);
             const uint32_t sQ = smem_u32(smem + C::kRes0), sO = smem_u32(smem + C::kRes1);
@@ -553,10 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (w >= p.num_items) break;
                 const BItem t = dq_item(p, w);
                 ok = mbar_wait(qd_full, k & 1, err, SITE_B_MMA_RES);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 for (int it = 0; it < t.n && ok; ++it, ++kc) {
                     const uint32_t st = kc & 1, ph = (kc >> 1) & 1;
                     ok = mbar_wait(&kv_full[st], ph, err, SITE_B_MMA_RING);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
                     // S = Q K^T and dP = dO V^T
@@ -564,29 +571,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                     const uint64_t vd = smem_desc_sw128(sV + st * C::kTileBytes, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kColS, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idS, kk > 0);
+                        mma_ss_w(tmem + kColS, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idS, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kColP, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idS, kk > 0);
-                    mma_commit(s_full);
+                        mma_ss_w(tmem + kColP, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idS, kk > 0);
+                    mma_commit_w(s_full);
                     ok = mbar_wait(p_full, pc & 1, err, SITE_B_MMA_P);
                     ++pc;
                     if (ok && it == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
                     // dQ += dS K (K MN-major: the contraction runs over keys)
                     const uint64_t kmn = smem_desc_sw128(sK + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), kmn + mnmajor_step(kk), idG,
+                        mma_ts_w(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), kmn + mnmajor_step(kk), idG,
                                (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&kv_empty[st]);
+                    mma_commit_w(&kv_empty[st]);
                 }
                 if (!ok) break;
-                mma_commit(qd_empty);
-                mma_commit(acc_full);
+                mma_commit_w(qd_empty);
+                mma_commit_w(acc_full);
             }
-            mma_commit(mma_done);
+            mma_commit_w(mma_done);
             mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE);
         }
     } else {
