@@ -62,7 +62,11 @@ struct Cfg {
     static constexpr uint32_t kQ = 0;                      // 2 Q tiles
     static constexpr uint32_t kK = 2 * kTileBytes;         // K ring
     static constexpr uint32_t kV = kK + kKStages * kTileBytes;  // V ring
-    static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
+    // One 128 x 64 swizzle atom of bias operands for the causal kernel: K-step 0
+    // holds ones (A side), K-steps 1 and 2 the per-head column bias of two items
+    // in flight (B side).
+    static constexpr uint32_t kAux = kV + kVStages * kTileBytes;
+    static constexpr uint32_t kBar = kAux + kChunkBytes;
     static constexpr uint32_t kSmem = kBar + 256 + 1024;   // barriers, TMEM slot, alignment slack
 };
 
@@ -109,6 +113,36 @@ __device__ __forceinline__ float rcp_approx(float x)
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// The causal plain kernel adds the column part of the bias, m log2(e) (k - k0),
+// on the tensor core: one more K-step whose A rows are (1, 1, 1, 0, ...) and
+// whose B row for key column c holds (m log2(e) c / c1) split into three bf16
+// terms (hi + mid + lo carries 24 bits), so S' = q.k + bias / c1 comes out of
+// the accumulator and the softmax only adds the row part nb.
+__device__ __forceinline__ bool use_aux_bias(const FwdParams &p, bool var) { return p.causal && !var; }
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Write row r of the column-bias operand (buffer `buf`: logical chunks 2 + 2 buf, 3 + 2 buf).
+template <int D>
+__device__ __forceinline__ void write_bias_row(uint8_t *aux, int r, int buf, float sl2, float c1)
+{
+    const float b = sl2 * static_cast<float>(r) / c1;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+    const float r1 = b - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+    const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+    const int j0 = 2 + 2 * buf;
+    uint8_t *row = aux + r * 128;
+    *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = make_uint4(w0, w1, 0u, 0u);
+    *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c)
@@ -198,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     uint64_t *o_empty = bars + 17;  // [2]
     uint64_t *mma_done = bars + 19; // [1]
     uint64_t *p_hi = bars + 20;     // [2] P of keys 64..127 written (p_full covers keys 0..63)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 22);
+    uint64_t *bias_full = bars + 22;  // [2] column-bias operand of item k written (buffer k & 1)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 24);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -219,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
         mbar_init(q_empty, 1);
         mbar_init(mma_done, 1);
+        mbar_init(&bias_full[0], 4);  // the slot-0 softmax warps
+        mbar_init(&bias_full[1], 4);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
@@ -227,6 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
+    }
+    if (use_aux_bias(p, VAR) && threadIdx.x < 2 * BM) {
+        // ones in logical 16-byte chunks 0-1 of every row (the A operand of the bias MMA)
+        const int r = threadIdx.x >> 1, j = threadIdx.x & 1;
+        const uint4 v = j == 0 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(smem + C::kAux + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -283,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t sQ = smem_u32(smem + C::kQ);
             const uint32_t sK = smem_u32(smem + C::kK);
             const uint32_t sV = smem_u32(smem + C::kV);
+            const bool aux = use_aux_bias(p, VAR);
+            const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
             uint32_t kc = 0, vc = 0;
             uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool ok = true;
@@ -292,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const Item t = decode_item(p, w);
                 const int last_slot = t.q1valid ? 1 : 0;
                 ok = mbar_wait(&q_full[0], k & 1, err, SITE_MMA_Q) && mbar_wait(&q_full[1], k & 1, err, SITE_MMA_Q);
+                if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_MMA_Q);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
 
@@ -308,6 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         const uint32_t step = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
                         mma_ss_w(dst, qd + step, kd + step, idS, kk > 0);
                     }
+                    // column bias: ones (K-step 0 of the aux atom) x this item's bias rows (K-step 1 + buf)
+                    if (aux) mma_ss_w(dst, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
                     mma_commit_w(&s_full[s]);
                 };
                 // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous;
@@ -397,6 +446,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int w = item_index(k);
             if (w >= p.num_items) break;
             const Item t = decode_item(p, w);
+            if (s == 0 && use_aux_bias(p, VAR)) {
+                // Column-bias operand, one row per thread, one item ahead: item 0's at the
+                // start, item k+1's at the start of item k (buffer (k+1) & 1; every MMA that
+                // read that buffer for item k-1 completed before this warp's epilogue of k-1).
+                auto publish = [&](int kk) {
+                    const int wn = item_index(kk);
+                    if (wn >= p.num_items) return;
+                    const Item tn = decode_item(p, wn);
+                    write_bias_row<D>(smem + C::kAux, r, kk & 1, p.slopes.log2e[tn.bh % p.H], p.c1);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bias_full[kk & 1]);
+                };
+                if (k == 0) publish(0);
+                publish(k + 1);
+            }
             if (s == 1 && !t.q1valid) continue;
             const int qt = 2 * t.qb + s;
             const int i = qt * BM + r;
@@ -448,6 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         }
                         if (clamp) b = fmaxf(b, p.clamp2);
                         x[c] = a + b;
+                    }
+                } else if (p.causal) {
+                    // the column part of the bias is already in S (see use_aux_bias)
+                    const float2 nbv = make_float2(nb, nb);
+#pragma unroll
+                    for (int u = 0; u < BN / 2; ++u) {
+                        const float2 xv = __ffma2_rn(
+                            make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, nbv);
+                        x[2 * u] = xv.x;
+                        x[2 * u + 1] = xv.y;
                     }
                 } else if (!sym) {
 #pragma unroll
