@@ -30,6 +30,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace alibi {
@@ -416,22 +418,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                         dk[u] = pack_bf16x2(dv[0], dv[1]);
                     }
                 } else {
+                    // one loop per (mask, bias form): the tile-uniform choices stay out of the element loop
+                    auto run = [&](auto diag_c, auto sym_c) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        float pv[2], dv[2];
+                        for (int u = 0; u < 32; ++u) {
+                            float pv[2], dv[2];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int c = 2 * u + e;
-                            const float tt = fmaf(sl2, static_cast<float>(c), base);
-                            const float b = p.causal ? -tt : -fabsf(tt);
-                            float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) - buf[c];
-                            if (diag && 64 * s + c < r) x = -INFINITY;  // query before key: masked
-                            pv[e] = ex2_approx(x);
-                            dv[e] = pv[e] * (__uint_as_float(draw[c]) - buf[64 + c]);
+                            for (int e = 0; e < 2; ++e) {
+                                const int c = 2 * u + e;
+                                const float tt = fmaf(sl2, static_cast<float>(c), base);
+                                const float b = decltype(sym_c)::value ? -fabsf(tt) : -tt;
+                                float x = fmaf(__uint_as_float(sraw[c]), p.c1, b - buf[c]);
+                                if (decltype(diag_c)::value && 64 * s + c < r) x = -INFINITY;  // query before key
+                                pv[e] = ex2_approx(x);
+                                dv[e] = pv[e] * (__uint_as_float(draw[c]) - buf[64 + c]);
+                            }
+                            pk[u] = pack_bf16x2(pv[0], pv[1]);
+                            dk[u] = pack_bf16x2(dv[0], dv[1]);
                         }
-                        pk[u] = pack_bf16x2(pv[0], pv[1]);
-                        dk[u] = pack_bf16x2(dv[0], dv[1]);
-                    }
+                    };
+                    if (!p.causal)
+                        run(std::false_type{}, std::true_type{});
+                    else if (diag)
+                        run(std::true_type{}, std::false_type{});
+                    else
+                        run(std::false_type{}, std::false_type{});
                 }
                 tmem_st32(lane_addr + kColS + 64 * s, pk);
                 tmem_st32(lane_addr + kColP + 64 * s, dk);
@@ -650,21 +661,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                         dk[u] = pack_bf16x2(dv[0], dv[1]);
                     }
                 } else {
+                    // one loop per (mask, bias form): the tile-uniform choices stay out of the element loop
+                    auto run = [&](auto diag_c, auto sym_c) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        float dv[2];
+                        for (int u = 0; u < 32; ++u) {
+                            float dv[2];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int c = 2 * u + e;
-                            const float tt = fmaf(sl2, static_cast<float>(c), nb);
-                            const float b = p.causal ? tt : -fabsf(tt);
-                            float x = fmaf(__uint_as_float(sraw[c]), p.c1, b) + nl;
-                            if (diag && 64 * s + c > r) x = -INFINITY;  // key after the query: masked
-                            const float pv = ex2_approx(x);
-                            dv[e] = pv * (__uint_as_float(draw[c]) - Di);
+                            for (int e = 0; e < 2; ++e) {
+                                const int c = 2 * u + e;
+                                const float tt = fmaf(sl2, static_cast<float>(c), nb);
+                                const float b = decltype(sym_c)::value ? -fabsf(tt) : tt;
+                                float x = fmaf(__uint_as_float(sraw[c]), p.c1, b + nl);
+                                if (decltype(diag_c)::value && 64 * s + c > r) x = -INFINITY;  // key after the query
+                                const float pv = ex2_approx(x);
+                                dv[e] = pv * (__uint_as_float(draw[c]) - Di);
+                            }
+                            dk[u] = pack_bf16x2(dv[0], dv[1]);
                         }
-                        dk[u] = pack_bf16x2(dv[0], dv[1]);
-                    }
+                    };
+                    if (!p.causal)
+                        run(std::false_type{}, std::true_type{});
+                    else if (diag)
+                        run(std::true_type{}, std::false_type{});
+                    else
+                        run(std::false_type{}, std::false_type{});
                 }
                 tmem_st32(lane_addr + kColS + 64 * s, dk);
                 tmem_wait_st();
