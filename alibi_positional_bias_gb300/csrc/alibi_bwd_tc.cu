@@ -61,7 +61,8 @@ struct BwdCfg {
     static constexpr uint32_t kRing0 = 2 * kTileBytes;           // Q / K, 2 stages
     static constexpr uint32_t kRing1 = 4 * kTileBytes;           // dO / V, 2 stages
     static constexpr uint32_t kStats = 6 * kTileBytes;           // dKdV: per warp 2 x (64 + 64) floats
-    static constexpr uint32_t kBar = kStats + 8 * 2 * 128 * 4;
+    static constexpr uint32_t kAux = kStats + 8 * 2 * 128 * 4;   // bias operands (ptx.cuh), one atom
+    static constexpr uint32_t kBar = kAux + kChunkBytes;
     static constexpr uint32_t kSmem = kBar + 256 + 1024;
 };
 
@@ -113,6 +114,11 @@ __device__ __forceinline__ float var_weight(const BwdParams &p, float mnat, floa
     *fac = f;
     return ex2_approx(a + b + nlse2);
 }
+
+// Causal plain kernels add the column part of the bias on the tensor core (the bias
+// operands of ptx.cuh): one more K-step after S = Q K^T (dQ; B row = key column c:
+// m log2(e) c / c1) or S^T = K Q^T (dK/dV; B row = query column c: -m log2(e) c / c1).
+__device__ __forceinline__ bool bwd_aux(const BwdParams &p, bool var) { return p.causal && !var; }
 
 enum : uint32_t {
     SITE_B_PROD_RES = 0x401, SITE_B_PROD_RING = 0x402, SITE_B_MMA_RES = 0x411, SITE_B_MMA_RING = 0x412,
@@ -221,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     uint64_t *acc_full = bars + 8;
     uint64_t *acc_empty = bars + 9;
     uint64_t *mma_done = bars + 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *bias_full = bars + 13;  // [2] column-bias operand of item k written (buffer k & 1)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t *err = p.err;
@@ -238,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);
         mbar_init(mma_done, 1);
+        mbar_init(&bias_full[0], 4);  // the first elementwise warpgroup
+        mbar_init(&bias_full[1], 4);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
@@ -247,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
+    }
+    if (bwd_aux(p, VAR) && threadIdx.x < 2 * BT) {
+        write_ones_chunk(smem + C::kAux, threadIdx.x >> 1, threadIdx.x & 1);
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -292,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const uint32_t sK = smem_u32(smem + C::kRes0), sV = smem_u32(smem + C::kRes1);
             const uint32_t sQ = smem_u32(smem + C::kRing0), sO = smem_u32(smem + C::kRing1);
             const uint64_t kd = smem_desc_sw128(sK, 16, 1024), vd = smem_desc_sw128(sV, 16, 1024);
+            const bool aux = bwd_aux(p, VAR);
+            const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
             uint32_t qc = 0, pc = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -299,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 if (w >= p.num_items) break;
                 const BItem t = dkdv_item(p, w);
                 ok = mbar_wait(kv_full, k & 1, err, SITE_B_MMA_RES);
+                if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 for (int it = 0; it < t.n && ok; ++it, ++qc) {
@@ -313,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss_w(tmem + kColS, kd + kmajor_step<D>(kk), qd + kmajor_step<D>(kk), idS, kk > 0);
+                    // column (query) bias: ones x this item's bias rows
+                    if (aux) mma_ss_w(tmem + kColS, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss_w(tmem + kColP, vd + kmajor_step<D>(kk), od + kmajor_step<D>(kk), idS, kk > 0);
@@ -351,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // key row of the tile
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        // per-warp double buffer of the 64 columns' LSE (base 2) and D
+        // per-warp double buffer of the 64 columns' -LSE (base 2) and -D
         float *stats = reinterpret_cast<float *>(smem + C::kStats) + (warp - 4) * 2 * 128;
         uint32_t s_cnt = 0;
         bool ok = true;
@@ -361,6 +379,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const BItem t = dkdv_item(p, w);
             const float sl2 = p.slopes.log2e[t.bh % p.H];
             const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
+            if (s == 0 && bwd_aux(p, VAR)) {
+                // column-bias rows (query column c: -m log2(e) c / c1), one item ahead
+                auto publish = [&](int kk) {
+                    const int wn = item_index(kk);
+                    if (wn >= p.num_items) return;
+                    const BItem tn = dkdv_item(p, wn);
+                    write_bias_row(smem + C::kAux, r, kk & 1, -p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bias_full[kk & 1]);
+                };
+                if (k == 0) publish(0);
+                publish(k + 1);
+            }
             // this lane's share of the column statistics of iteration `it` (prefetched one ahead)
             auto fetch = [&](int it, float (&v)[4]) {
                 const int q0 = dkdv_qtile(p, t, it) * BT + 64 * s;
@@ -368,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 for (int h = 0; h < 2; ++h) {
                     const int i = q0 + lane + 32 * h;
                     const bool in = i < p.N;
-                    v[h] = in ? p.lse[rowbase + i] * kLog2e : INFINITY;  // past N: weight 0
-                    v[2 + h] = in ? p.dsum[rowbase + i] : 0.f;
+                    v[h] = in ? -p.lse[rowbase + i] * kLog2e : -INFINITY;  // -LSE log2(e); past N: weight 0
+                    v[2 + h] = in ? -p.dsum[rowbase + i] : 0.f;              // -D
                 }
             };
             float pre[4];
@@ -409,15 +441,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                             const int c = 2 * u + e;
                             float f;
                             float w = var_weight(p, mnat, sl2, __uint_as_float(sraw[c]),
-                                                 fabsf(di + static_cast<float>(c)), -buf[c], &f);
+                                                 fabsf(di + static_cast<float>(c)), buf[c], &f);
                             if (diag && 64 * s + c < r) w = 0.f;  // query before key: masked
                             pv[e] = w;
-                            dv[e] = w * (__uint_as_float(draw[c]) - buf[64 + c]) * f;
+                            dv[e] = w * (__uint_as_float(draw[c]) + buf[64 + c]) * f;
                         }
                         pk[u] = pack_bf16x2(pv[0], pv[1]);
                         dk[u] = pack_bf16x2(dv[0], dv[1]);
                     }
                 } else {
+                    // causal: the column bias is already in S^T (bwd_aux); what is left per
+                    // element is c1 S' + (row part) - LSE_c, the exponential, and P (dP - D)
+                    const float rowpart = -sl2 * static_cast<float>((qt - t.tile) * BT - r);
+                    auto run_aux = [&](auto diag_c) {
+                        const float2 c1v = make_float2(p.c1, p.c1), rp = make_float2(rowpart, rowpart);
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            const float2 nl = *reinterpret_cast<const float2 *>(buf + 2 * u);
+                            const float2 nd = *reinterpret_cast<const float2 *>(buf + 64 + 2 * u);
+                            float2 xv = __fadd2_rn(
+                                __ffma2_rn(make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])),
+                                           c1v, rp),
+                                nl);
+                            if (decltype(diag_c)::value) {  // query before key: masked
+                                if (64 * s + 2 * u < r) xv.x = -INFINITY;
+                                if (64 * s + 2 * u + 1 < r) xv.y = -INFINITY;
+                            }
+                            const float2 pv = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
+                            const float2 dv = __fmul2_rn(
+                                pv, __fadd2_rn(make_float2(__uint_as_float(draw[2 * u]), __uint_as_float(draw[2 * u + 1])),
+                                               nd));
+                            pk[u] = pack_bf16x2(pv.x, pv.y);
+                            dk[u] = pack_bf16x2(dv.x, dv.y);
+                        }
+                    };
                     // one loop per (mask, bias form): the tile-uniform choices stay out of the element loop
                     auto run = [&](auto diag_c, auto sym_c) {
 #pragma unroll
@@ -428,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                                 const int c = 2 * u + e;
                                 const float tt = fmaf(sl2, static_cast<float>(c), base);
                                 const float b = decltype(sym_c)::value ? -fabsf(tt) : -tt;
-                                float x = fmaf(__uint_as_float(sraw[c]), p.c1, b - buf[c]);
+                                float x = fmaf(__uint_as_float(sraw[c]), p.c1, b + buf[c]);
                                 if (decltype(diag_c)::value && 64 * s + c < r) x = -INFINITY;  // query before key
                                 pv[e] = ex2_approx(x);
-                                dv[e] = pv[e] * (__uint_as_float(draw[c]) - buf[64 + c]);
+                                dv[e] = pv[e] * (__uint_as_float(draw[c]) + buf[64 + c]);
                             }
                             pk[u] = pack_bf16x2(pv[0], pv[1]);
                             dk[u] = pack_bf16x2(dv[0], dv[1]);
@@ -440,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                     if (!p.causal)
                         run(std::false_type{}, std::true_type{});
                     else if (diag)
-                        run(std::true_type{}, std::false_type{});
+                        run_aux(std::true_type{});
                     else
-                        run(std::false_type{}, std::false_type{});
+                        run_aux(std::false_type{});
                 }
                 tmem_st32(lane_addr + kColS + 64 * s, pk);
                 tmem_st32(lane_addr + kColP + 64 * s, dk);
@@ -494,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     uint64_t *acc_full = bars + 8;
     uint64_t *acc_empty = bars + 9;
     uint64_t *mma_done = bars + 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *bias_full = bars + 13;  // [2] column-bias operand of item k written (buffer k & 1)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t *err = p.err;
@@ -511,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);
         mbar_init(mma_done, 1);
+        mbar_init(&bias_full[0], 4);  // the first elementwise warpgroup
+        mbar_init(&bias_full[1], 4);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
@@ -520,6 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
+    }
+    if (bwd_aux(p, VAR) && threadIdx.x < 2 * BT) {
+        write_ones_chunk(smem + C::kAux, threadIdx.x >> 1, threadIdx.x & 1);
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -562,6 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             const uint32_t sQ = smem_u32(smem + C::kRes0), sO = smem_u32(smem + C::kRes1);
             const uint32_t sK = smem_u32(smem + C::kRing0), sV = smem_u32(smem + C::kRing1);
             const uint64_t qd = smem_desc_sw128(sQ, 16, 1024), od = smem_desc_sw128(sO, 16, 1024);
+            const bool aux = bwd_aux(p, VAR);
+            const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
             uint32_t kc = 0, pc = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -569,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (w >= p.num_items) break;
                 const BItem t = dq_item(p, w);
                 ok = mbar_wait(qd_full, k & 1, err, SITE_B_MMA_RES);
+                if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 for (int it = 0; it < t.n && ok; ++it, ++kc) {
@@ -583,6 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss_w(tmem + kColS, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idS, kk > 0);
+                    // column (key) bias: ones x this item's bias rows
+                    if (aux) mma_ss_w(tmem + kColS, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss_w(tmem + kColP, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idS, kk > 0);
@@ -621,6 +690,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             if (w >= p.num_items) break;
             const BItem t = dq_item(p, w);
             const float sl2 = p.slopes.log2e[t.bh % p.H];
+            if (s == 0 && bwd_aux(p, VAR)) {
+                // column-bias rows (key column c: m log2(e) c / c1), one item ahead
+                auto publish = [&](int kk) {
+                    const int wn = item_index(kk);
+                    if (wn >= p.num_items) return;
+                    const BItem tn = dq_item(p, wn);
+                    write_bias_row(smem + C::kAux, r, kk & 1, p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bias_full[kk & 1]);
+                };
+                if (k == 0) publish(0);
+                publish(k + 1);
+            }
             const int i = t.tile * BT + r;
             const bool valid = i < p.N;
             const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
@@ -661,6 +744,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                         dk[u] = pack_bf16x2(dv[0], dv[1]);
                     }
                 } else {
+                    // causal: the column bias is already in S (bwd_aux): exponent c1 S' + (nb - LSE)
+                    const float rowoff = -sl2 * static_cast<float>(i - it * BT) + nl;
+                    auto run_aux = [&](auto diag_c) {
+                        const float2 c1v = make_float2(p.c1, p.c1), ro = make_float2(rowoff, rowoff);
+                        const float2 nD = make_float2(-Di, -Di);
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            float2 xv = __ffma2_rn(
+                                make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, ro);
+                            if (decltype(diag_c)::value) {  // key after the query: masked
+                                if (64 * s + 2 * u > r) xv.x = -INFINITY;
+                                if (64 * s + 2 * u + 1 > r) xv.y = -INFINITY;
+                            }
+                            const float2 pv = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
+                            const float2 dv = __fmul2_rn(
+                                pv, __fadd2_rn(make_float2(__uint_as_float(draw[2 * u]), __uint_as_float(draw[2 * u + 1])),
+                                               nD));
+                            dk[u] = pack_bf16x2(dv.x, dv.y);
+                        }
+                    };
                     // one loop per (mask, bias form): the tile-uniform choices stay out of the element loop
                     auto run = [&](auto diag_c, auto sym_c) {
 #pragma unroll
@@ -682,9 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                     if (!p.causal)
                         run(std::false_type{}, std::true_type{});
                     else if (diag)
-                        run(std::true_type{}, std::false_type{});
+                        run_aux(std::true_type{});
                     else
-                        run(std::false_type{}, std::false_type{});
+                        run_aux(std::false_type{});
                 }
                 tmem_st32(lane_addr + kColS + 64 * s, dk);
                 tmem_wait_st();

@@ -116,34 +116,10 @@ __device__ __forceinline__ float rcp_approx(float x)
 }
 
 // The causal plain kernel adds the column part of the bias, m log2(e) (k - k0),
-// on the tensor core: one more K-step whose A rows are (1, 1, 1, 0, ...) and
-// whose B row for key column c holds (m log2(e) c / c1) split into three bf16
-// terms (hi + mid + lo carries 24 bits), so S' = q.k + bias / c1 comes out of
-// the accumulator and the softmax only adds the row part nb.
+// on the tensor core (the bias operands of ptx.cuh; B row c = m log2(e) c / c1),
+// so S' = q.k + bias / c1 comes out of the accumulator and the softmax only adds
+// the row part nb.
 __device__ __forceinline__ bool use_aux_bias(const FwdParams &p, bool var) { return p.causal && !var; }
-
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Write row r of the column-bias operand (buffer `buf`: logical chunks 2 + 2 buf, 3 + 2 buf).
-template <int D>
-__device__ __forceinline__ void write_bias_row(uint8_t *aux, int r, int buf, float sl2, float c1)
-{
-    const float b = sl2 * static_cast<float>(r) / c1;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(b);
-    const float r1 = b - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-    const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
-    const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
-    const int j0 = 2 + 2 * buf;
-    uint8_t *row = aux + r * 128;
-    *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = make_uint4(w0, w1, 0u, 0u);
-    *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-}
 
 __device__ __forceinline__ float max3f(float a, float b, float c)
 {
@@ -267,9 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     }
     if (use_aux_bias(p, VAR) && threadIdx.x < 2 * BM) {
         // ones in logical 16-byte chunks 0-1 of every row (the A operand of the bias MMA)
-        const int r = threadIdx.x >> 1, j = threadIdx.x & 1;
-        const uint4 v = j == 0 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(smem + C::kAux + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+        write_ones_chunk(smem + C::kAux, threadIdx.x >> 1, threadIdx.x & 1);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -454,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int wn = item_index(kk);
                     if (wn >= p.num_items) return;
                     const Item tn = decode_item(p, wn);
-                    write_bias_row<D>(smem + C::kAux, r, kk & 1, p.slopes.log2e[tn.bh % p.H], p.c1);
+                    write_bias_row(smem + C::kAux, r, kk & 1, p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bias_full[kk & 1]);

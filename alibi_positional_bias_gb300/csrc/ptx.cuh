@@ -274,6 +274,43 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
            | ((M >> 4) << 24);   // M / 16
 }
 
+// ------------------------------------------------- bias operands in smem
+//
+// A column bias that is the same for every tile of a head can be added by the
+// tensor core: one more K=16 step whose A rows are (1, 1, 1, 0, ...) and whose B
+// row for column c holds the bias value split into three bf16 terms (hi, mid,
+// lo: 24 bits). Both operands live in one 128 x 64 bf16 atom with the 128-byte
+// swizzle (the TMA layout: 16-byte chunk j of row r at chunk j ^ (r & 7)):
+// logical chunks 0-1 hold the ones, chunks 2 + 2b and 3 + 2b bias buffer b.
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Row r of the ones operand (logical chunks 0 and 1; write both halves: j = 0, 1).
+__device__ __forceinline__ void write_ones_chunk(uint8_t *aux, int r, int j)
+{
+    const uint4 v = j == 0 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(aux + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+}
+
+// Row r of bias buffer `buf`: the value b as hi + mid + lo bf16 terms.
+__device__ __forceinline__ void write_bias_row(uint8_t *aux, int r, int buf, float b)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+    const float r1 = b - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+    const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+    const int j0 = 2 + 2 * buf;
+    uint8_t *row = aux + r * 128;
+    *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = make_uint4(w0, w1, 0u, 0u);
+    *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // ---------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float ex2_approx(float x)
