@@ -381,6 +381,7 @@ def run_native(args):
     tile_flops = 4.0 * 128 * 128 * wp.d  # QK^T + PV of one 128 x 128 tile
     # -------------------- exact underflow-tile skipping, same inputs, own timing
     skip = noncausal = steep = backward = None
+    others = None
     if do_pre:
         tiles_run, tiles_all = tiles_kept(ab.alibi_attn_skip_plan(q, k).cpu().numpy())
         t_skip = timed_ms(lambda: ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True))
@@ -424,6 +425,21 @@ def run_native(args):
                     "launches": 3,  # D = rowsum(dO o O), dK/dV kernel, dQ kernel
                     "peak_source": f"bf16 dense burst, {peaks['source']}"}
         del do_b, gq, gk, gv
+
+        # -------------------- the other prefill configurations (same kernel, own inputs)
+        others = {}
+        for name in ("heads6_n1024", "layer_n2048"):
+            wo = gen.WORKLOADS[name]
+            to = [torch.empty(wo.shapes()[i], dtype=torch.bfloat16, device=dev) for i in range(3)]
+            for i, t in enumerate(to):
+                gen.fill_device(wo, i, t)
+            oo = torch.empty_like(to[0])
+            lo = torch.empty((wo.B, wo.H, wo.N), dtype=torch.float32, device=dev)
+            t_o = timed_ms(lambda: ab.alibi_attn_fwd(*to, out=oo, lse=lo, stream=stream))
+            tf = prefill_flops(wo) / (t_o / 1e3) / 1e12
+            others[name] = {"shape": f"B={wo.B} H={wo.H} N={wo.N} d={wo.d}", "ms": t_o, "tflops": world * tf,
+                            "frac": tf / peaks["bf16_tflops"]}
+            del to, oo, lo
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
@@ -544,6 +560,7 @@ def run_native(args):
         "prefill_noncausal": noncausal,
         "prefill_steep_slopes": steep,
         "backward": backward,
+        "prefill_other_configs": others,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
