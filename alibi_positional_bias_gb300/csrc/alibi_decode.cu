@@ -8,24 +8,30 @@
 // 2608.03994), App. B.1, evaluated online and merged across splits.
 //
 // Memory-bound design: the cache is streamed once with 16-byte non-caching
-// loads. A half-warp owns one key row (16 lanes x 8 bf16 = 256 bytes = d 128),
-// so a warp-wide load covers two adjacent rows (512 contiguous bytes). Each
-// warp issues 16 K and 16 V loads (8 keys per half-warp) before using any of
-// them, keeping ~8 KB per warp in flight. Grid = (splits, B*H); each CTA (8
-// warps) streams a contiguous slice of the cache, merges its warps' partial
-// softmaxes in shared memory, and either writes the output (one split) or an
-// fp32 partial (m, l, o[d]) that a second kernel merges.
+// loads. A group of d/8 lanes owns one key row (8 bf16 per lane: 16 lanes for
+// d = 128, 8 for 64, 4 for 32, 2 for 16), so a warp-wide load covers 32/(d/8)
+// adjacent rows (512 contiguous bytes). Each lane issues 8 K and 8 V loads
+// before using them, keeping ~8 KB per warp in flight at every d. Grid =
+// (splits, B*H); each CTA (8 warps) streams a contiguous slice of the cache,
+// merges its warps' partial softmaxes in shared memory, and either writes the
+// output (one split) or an fp32 partial (m, l, o[d]) that a second kernel
+// merges.
 
 #include "ptx.cuh"
 
 namespace alibi {
 namespace {
 
-constexpr int kDecodeD = 128;
 constexpr int kWarps = 8;
-constexpr int kKeysPerHalf = 8;               // keys per half-warp per step
-constexpr int kKeysPerWarp = 2 * kKeysPerHalf;  // 16
-constexpr int kPartStride = kDecodeD + 4;     // floats per partial: m, l, pad, pad, o[d]
+constexpr int kKeysPerGroup = 8;  // keys per lane group per step
+
+template <int D>
+struct DecCfg {
+    static constexpr int kLanesPerRow = D / 8;              // 8 bf16 per lane
+    static constexpr int kGroups = 32 / kLanesPerRow;       // key rows per warp-wide load
+    static constexpr int kKeysPerWarp = kGroups * kKeysPerGroup;
+    static constexpr int kPartStride = D + 4;               // floats per partial: m, l, pad, pad, o[d]
+};
 
 struct DecodeParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -55,13 +61,16 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_constant__ DecodeParams p)
 {
+    using C = DecCfg<D>;
+    constexpr int LPR = C::kLanesPerRow;
     __shared__ float sm_m[kWarps], sm_l[kWarps];
-    __shared__ float sm_o[kWarps][kDecodeD];
+    __shared__ float sm_o[kWarps][D];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = lane >> 4, l16 = lane & 15;
+    const int half = lane / LPR, l16 = lane % LPR;  // lane group (key row) and slice within the row
     const int bh = blockIdx.y, split = blockIdx.x;
     const int h = bh % p.H;
     const float sl2 = p.slopes.log2e[h];
@@ -71,48 +80,46 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
 
     // this lane's 8 query elements (d slice [8 l16, 8 l16 + 8)), pre-scaled to log2 units
     float qf[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(p.q + static_cast<size_t>(bh) * kDecodeD + 8 * l16), qf);
+    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(p.q + static_cast<size_t>(bh) * D + 8 * l16), qf);
 #pragma unroll
     for (int t = 0; t < 8; ++t) qf[t] *= p.c1;
 
-    const __nv_bfloat16 *kbase = p.k + static_cast<size_t>(bh) * p.L * kDecodeD + 8 * l16;
-    const __nv_bfloat16 *vbase = p.v + static_cast<size_t>(bh) * p.L * kDecodeD + 8 * l16;
+    const __nv_bfloat16 *kbase = p.k + static_cast<size_t>(bh) * p.L * D + 8 * l16;
+    const __nv_bfloat16 *vbase = p.v + static_cast<size_t>(bh) * p.L * D + 8 * l16;
 
     float m = -INFINITY, l = 0.f, o[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) o[t] = 0.f;
 
-    for (int blk = kbeg + warp * kKeysPerWarp; blk < kend; blk += kWarps * kKeysPerWarp) {
-        uint4 kr[kKeysPerHalf], vr[kKeysPerHalf];
+    for (int blk = kbeg + warp * C::kKeysPerWarp; blk < kend; blk += kWarps * C::kKeysPerWarp) {
+        uint4 kr[kKeysPerGroup], vr[kKeysPerGroup];
 #pragma unroll
-        for (int u = 0; u < kKeysPerHalf; ++u) {
-            const int key = blk + 2 * u + half;
+        for (int u = 0; u < kKeysPerGroup; ++u) {
+            const int key = blk + C::kGroups * u + half;
             if (key < kend) {
-                kr[u] = ld_stream(kbase + static_cast<size_t>(key) * kDecodeD);
-                vr[u] = ld_stream(vbase + static_cast<size_t>(key) * kDecodeD);
+                kr[u] = ld_stream(kbase + static_cast<size_t>(key) * D);
+                vr[u] = ld_stream(vbase + static_cast<size_t>(key) * D);
             } else {
                 kr[u] = make_uint4(0, 0, 0, 0);
                 vr[u] = make_uint4(0, 0, 0, 0);
             }
         }
-        float x[kKeysPerHalf];
+        float x[kKeysPerGroup];
         float mt = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < kKeysPerHalf; ++u) {
+        for (int u = 0; u < kKeysPerGroup; ++u) {
             float kf[8];
             bf16x8_to_f32(kr[u], kf);
             float dot = 0.f;
 #pragma unroll
             for (int t = 0; t < 8; ++t) dot = fmaf(qf[t], kf[t], dot);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 8);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-            const int key = blk + 2 * u + half;
+#pragma unroll
+            for (int off = LPR / 2; off; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+            const int key = blk + C::kGroups * u + half;
             x[u] = (key < kend) ? fmaf(-sl2, static_cast<float>(pos - key), dot) : -INFINITY;
             mt = fmaxf(mt, x[u]);
         }
-        if (mt > -INFINITY) {  // this half-warp saw at least one key in range
+        if (mt > -INFINITY) {  // this lane group saw at least one key in range
             const float mn = fmaxf(m, mt);
             const float alpha = ex2_approx(m - mn);  // 0 while m is still -inf
             m = mn;
@@ -120,7 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
 #pragma unroll
             for (int t = 0; t < 8; ++t) o[t] *= alpha;
 #pragma unroll
-            for (int u = 0; u < kKeysPerHalf; ++u) {
+            for (int u = 0; u < kKeysPerGroup; ++u) {
                 const float pu = ex2_approx(x[u] - m);
                 l += pu;
                 float vf[8];
@@ -131,22 +138,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
         }
     }
 
-    // merge the two half-warps (lanes l16 and l16 + 16 own the same d slice)
-    {
-        const float mo = __shfl_xor_sync(0xffffffffu, m, 16);
-        const float lo = __shfl_xor_sync(0xffffffffu, l, 16);
+    // merge the lane groups (lanes l16 + LPR g own the same d slice for every g)
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, off);
         const float mn = fmaxf(m, mo);
         const float a = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
         const float b = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mn);
         l = l * a + lo * b;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const float oo = __shfl_xor_sync(0xffffffffu, o[t], 16);
+            const float oo = __shfl_xor_sync(0xffffffffu, o[t], off);
             o[t] = o[t] * a + oo * b;
         }
         m = mn;
     }
-    if (lane < 16) {
+    if (lane < LPR) {
 #pragma unroll
         for (int t = 0; t < 8; ++t) sm_o[warp][8 * l16 + t] = o[t];
         if (lane == 0) {
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
         }
     }
     __syncthreads();
-    if (threadIdx.x < kDecodeD) {
+    if (threadIdx.x < D) {
         const int t = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
@@ -168,9 +176,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
             O = fmaf(sm_o[w][t], a, O);
         }
         if (p.splits == 1) {
-            p.out[static_cast<size_t>(bh) * kDecodeD + t] = __float2bfloat16_rn(O / Lsum);
+            p.out[static_cast<size_t>(bh) * D + t] = __float2bfloat16_rn(O / Lsum);
         } else {
-            float *dst = p.part + (static_cast<size_t>(bh) * p.splits + split) * kPartStride;
+            float *dst = p.part + (static_cast<size_t>(bh) * p.splits + split) * C::kPartStride;
             if (t == 0) {
                 dst[0] = M;
                 dst[1] = Lsum;
@@ -180,20 +188,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
     }
 }
 
-// One warp per (b, h): merge the splits' partial softmaxes.
+// One warp per (b, h): merge the splits' partial softmaxes (lane t covers o[4t .. 4t + 3]).
+template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restrict__ part,
                                                            __nv_bfloat16 *__restrict__ out, int BH, int splits)
 {
+    constexpr int kStride = DecCfg<D>::kPartStride;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= BH) return;
-    const float *base = part + static_cast<size_t>(warp) * splits * kPartStride;
+    const float *base = part + static_cast<size_t>(warp) * splits * kStride;
     float M = -INFINITY;
-    for (int s = lane; s < splits; s += 32) M = fmaxf(M, base[s * kPartStride]);
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, base[s * kStride]);
 #pragma unroll
     for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (4 * lane >= D) return;
     float Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < splits; ++s) {
-        const float *ps = base + s * kPartStride;
+        const float *ps = base + s * kStride;
         const float ms = ps[0];
         const float a = (ms == -INFINITY) ? 0.f : ex2_approx(ms - M);
         Lsum = fmaf(ps[1], a, Lsum);
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restri
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t *>(&r0);
     pk.y = *reinterpret_cast<uint32_t *>(&r1);
-    *reinterpret_cast<uint2 *>(out + static_cast<size_t>(warp) * kDecodeD + 4 * lane) = pk;
+    *reinterpret_cast<uint2 *>(out + static_cast<size_t>(warp) * D + 4 * lane) = pk;
 }
 
 }  // namespace
@@ -226,14 +237,18 @@ int decode_splits(int BH, int L)
     return splits;
 }
 
-size_t decode_partials_bytes(int BH, int splits)
+size_t decode_partials_bytes(int BH, int splits, int d)
 {
-    return splits > 1 ? static_cast<size_t>(BH) * splits * kPartStride * sizeof(float) : 0;
+    return splits > 1 ? static_cast<size_t>(BH) * splits * (d + 4) * sizeof(float) : 0;
 }
 
-cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L,
-                               const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
+bool decode_supports(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+template <int D>
+static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L,
+                                   const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
 {
+    using C = DecCfg<D>;
     DecodeParams p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(kc);
@@ -244,32 +259,44 @@ cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, vo
     p.L = L;
     p.splits = splits;
     p.chunk = (L + splits - 1) / splits;
-    p.chunk = (p.chunk + kKeysPerWarp - 1) / kKeysPerWarp * kKeysPerWarp;
-    p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(kDecodeD));
+    p.chunk = (p.chunk + C::kKeysPerWarp - 1) / C::kKeysPerWarp * C::kKeysPerWarp;
+    p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     p.slopes = slopes;
     const int BH = B * H;
     // recompute splits so that no split is empty after rounding the chunk
     p.splits = (L + p.chunk - 1) / p.chunk;
     if (p.splits > splits) return cudaErrorInvalidValue;
     dim3 grid(p.splits, BH);
-    decode_kernel<<<grid, kWarps * 32, 0, stream>>>(p);
+    decode_kernel<D><<<grid, kWarps * 32, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;
-    decode_merge_kernel<<<(BH + 3) / 4, 128, 0, stream>>>(partials, p.out, BH, p.splits);
+    decode_merge_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(partials, p.out, BH, p.splits);
     return cudaGetLastError();
+}
+
+cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
+                               const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
+{
+    switch (d) {
+        case 128: return launch_decode_d<128>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
+        case 64: return launch_decode_d<64>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
+        case 32: return launch_decode_d<32>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
+        case 16: return launch_decode_d<16>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
                           const Slopes &slopes, cudaStream_t stream)
 {
-    if (d != kDecodeD) return cudaErrorInvalidValue;
+    if (!decode_supports(d)) return cudaErrorInvalidValue;
     const int BH = B * H;
     const int splits = decode_splits(BH, L);
-    if (splits == 1) return launch_decode_with(q, kc, vc, out, B, H, L, slopes, 1, nullptr, stream);
+    if (splits == 1) return launch_decode_with(q, kc, vc, out, B, H, L, d, slopes, 1, nullptr, stream);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, decode_partials_bytes(BH, splits), decode_pool(), stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, decode_partials_bytes(BH, splits, d), decode_pool(), stream);
     if (e != cudaSuccess) return e;
-    e = launch_decode_with(q, kc, vc, out, B, H, L, slopes, splits, static_cast<float *>(ws), stream);
+    e = launch_decode_with(q, kc, vc, out, B, H, L, d, slopes, splits, static_cast<float *>(ws), stream);
     cudaError_t f = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : f;
 }

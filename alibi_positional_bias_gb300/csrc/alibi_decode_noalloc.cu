@@ -62,17 +62,17 @@ extern "C" int alibi_attn_decode_noalloc(const void *q, const void *kcache, cons
     if (B < 1 || H < 1 || L < 1 || d < 1) return ALIBI_ERR_INVALID;
     if (H > kMaxHeads || L > (1 << 24) || static_cast<long long>(B) * H > (1LL << 31) - 1)
         return ALIBI_ERR_UNSUPPORTED;
-    if (d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (!decode_supports(d)) return ALIBI_ERR_UNSUPPORTED;
     // same split plan as alibi_attn_decode, so both give the same result
     const int splits = decode_splits(B * H, L);
-    if (decode_partials_bytes(B * H, splits) > kNoAllocScratchBytes) return ALIBI_ERR_UNSUPPORTED;
+    if (decode_partials_bytes(B * H, splits, d) > kNoAllocScratchBytes) return ALIBI_ERR_UNSUPPORTED;
     float *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return ALIBI_ERR_CUDA;
     Slopes s;
     fill_slopes(H, &s);
     // Every partial the merge reads is written earlier in the same call, so the
     // buffer needs no clearing; what the previous call left there is overwritten.
-    const cudaError_t e = launch_decode_with(q, kcache, vcache, out, B, H, L, s, splits,
+    const cudaError_t e = launch_decode_with(q, kcache, vcache, out, B, H, L, d, s, splits,
                                              splits > 1 ? scratch : nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ALIBI_OK : ALIBI_ERR_CUDA;
 }

@@ -76,6 +76,7 @@ struct FwdParams {
     float *lse;
     uint32_t *err;
     int N, BH, H, NQB, NQT, num_items;
+    int dr;  // the tensors' head size (<= D: the D = 64 kernel also serves d = 16 and 32)
     int causal;  // 1: keys j <= i only; 0: every key, distance |i - j|
     float c1;  // log2(e) / sqrt(d)
     const int2 *plan;  // optional: work order (item, first KV tile); null = dense, nominal order
@@ -592,9 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
             const float inv_l = 1.0f / l;
             const bool valid = i < p.N;
-            __nv_bfloat16 *orow = p.out + (static_cast<size_t>(t.bh) * p.N + (valid ? i : 0)) * D;
+            __nv_bfloat16 *orow = p.out + (static_cast<size_t>(t.bh) * p.N + (valid ? i : 0)) * p.dr;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
+                if (c * 32 >= p.dr) break;  // columns past a smaller head size are zero and not stored
                 uint32_t o[32];
                 tmem_ld32(lane_addr + 256 + s * 128 + c * 32, o);
                 tmem_wait_ld();
@@ -604,8 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv_l, __uint_as_float(o[2 * u + 1]) * inv_l);
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    const int n16 = min(4, (p.dr - c * 32) / 8);  // 16-byte stores in this chunk
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                    for (int u = 0; u < 4; ++u)
+                        if (u < n16) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
                 }
             }
             tc_fence_before();
@@ -625,17 +629,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
 }  // namespace
 
+// dr <= D is the tensors' head size: for dr < 64 the D = 64 kernel runs with a
+// 64-column TMA box over dr-column rows, so the columns past dr arrive as zeros
+// (they add nothing to S, and the matching columns of O come out zero and are
+// not stored).
 template <int D, bool VAR>
 static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, void *out, float *lse, int B,
-                                   int H, int N, int causal, const Slopes &slopes, const int2 *plan, unsigned int variant,
-                                   float clamp_min, float softcap_z, cudaStream_t stream)
+                                   int H, int N, int dr, int causal, const Slopes &slopes, const int2 *plan,
+                                   unsigned int variant, float clamp_min, float softcap_z, cudaStream_t stream)
 {
     using C = Cfg<D>;
     FwdParams p;
     const uint64_t BH = static_cast<uint64_t>(B) * H;
-    if (!encode_tmap_bf16_3d(&p.tq, q, D, N, BH, 64, BM) || !encode_tmap_bf16_3d(&p.tk, k, D, N, BH, 64, BN) ||
-        !encode_tmap_bf16_3d(&p.tv, v, D, N, BH, 64, BN))
+    if (!encode_tmap_bf16_3d(&p.tq, q, dr, N, BH, 64, BM) || !encode_tmap_bf16_3d(&p.tk, k, dr, N, BH, 64, BN) ||
+        !encode_tmap_bf16_3d(&p.tv, v, dr, N, BH, 64, BN))
         return cudaErrorInvalidValue;
+    p.dr = dr;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
     p.err = device_status_word();
@@ -647,12 +656,12 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     p.NQB = (p.NQT + 1) / 2;
     p.num_items = p.NQB * p.BH;
     p.causal = causal;
-    p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(dr));
     p.slopes = slopes;
     p.plan = plan;
     p.variant = variant & (kFwdClamp | kFwdLogDist | kFwdSoftcap);
     p.clamp2 = clamp_min * 1.4426950408889634f;
-    p.cap_k = (variant & kFwdSoftcap) ? 2.0f * 1.4426950408889634f / (sqrtf(static_cast<float>(D)) * softcap_z) : 0.f;
+    p.cap_k = (variant & kFwdSoftcap) ? 2.0f * 1.4426950408889634f / (sqrtf(static_cast<float>(dr)) * softcap_z) : 0.f;
     p.cap_zl = softcap_z * 1.4426950408889634f;
 
     static bool attr_set = false;  // per process; the attribute is per function
@@ -677,17 +686,17 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out
                           int d, int causal, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
                           cudaStream_t stream)
 {
-    if (d != 128 && d != 64) return cudaErrorInvalidValue;
+    if (d != 128 && d != 64 && d != 32 && d != 16) return cudaErrorInvalidValue;
     auto run = [&](const int2 *plan) {
         const bool var = (flags & (kFwdClamp | kFwdLogDist | kFwdSoftcap)) != 0;
         if (d == 128)
-            return var ? launch_fwd_tc_d<128, true>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min,
-                                                    softcap_z, stream)
-                       : launch_fwd_tc_d<128, false>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min,
-                                                     softcap_z, stream);
-        return var ? launch_fwd_tc_d<64, true>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min, softcap_z,
-                                               stream)
-                   : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, causal, slopes, plan, flags, clamp_min,
+            return var ? launch_fwd_tc_d<128, true>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags,
+                                                    clamp_min, softcap_z, stream)
+                       : launch_fwd_tc_d<128, false>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags,
+                                                     clamp_min, softcap_z, stream);
+        return var ? launch_fwd_tc_d<64, true>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags, clamp_min,
+                                               softcap_z, stream)
+                   : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags, clamp_min,
                                                 softcap_z, stream);
     };
     if (!(flags & kFwdSkipUnderflow)) return run(nullptr);

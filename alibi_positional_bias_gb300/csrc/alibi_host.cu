@@ -246,7 +246,7 @@ int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, fl
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
     if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
-    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
     const unsigned int known = ALIBI_FWD_SKIP_UNDERFLOW | ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP;
     if (flags & ~known) return ALIBI_ERR_INVALID;
     if ((flags & ALIBI_FWD_CLAMP) && !(clamp_min < 0.0f)) return ALIBI_ERR_INVALID;
@@ -317,7 +317,7 @@ int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int 
     if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(first_tile) & 3u)) return ALIBI_ERR_INVALID;
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
-    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
     if (slopes && !slopes_ok(H, slopes)) return ALIBI_ERR_INVALID;
     Slopes s;
     if (slopes)
@@ -361,7 +361,7 @@ int alibi_attn_decode(const void *q, const void *kcache, const void *vcache, voi
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out)) return ALIBI_ERR_INVALID;
     int st = check_dims(B, H, L, d);
     if (st != ALIBI_OK) return st;
-    if (d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (!decode_supports(d)) return ALIBI_ERR_UNSUPPORTED;
     Slopes s;
     fill_slopes(H, &s);
     return to_status(launch_decode(q, kcache, vcache, out, B, H, L, d, s, static_cast<cudaStream_t>(stream)));
@@ -371,7 +371,7 @@ int alibi_attn_decode_splits(int B, int H, int L, int d)
 {
     int st = check_dims(B, H, L, d);
     if (st != ALIBI_OK) return st;
-    if (d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (!decode_supports(d)) return ALIBI_ERR_UNSUPPORTED;
     return decode_splits(B * H, L);
 }
 
@@ -401,7 +401,7 @@ int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N,
     if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(counts) & 7u)) return ALIBI_ERR_INVALID;
     int st = check_dims(B, H, N, d);
     if (st != ALIBI_OK) return st;
-    if (d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
     if (!std::isfinite(tau)) return ALIBI_ERR_INVALID;
     Slopes s;
     fill_slopes(H, &s);

@@ -265,6 +265,10 @@ cudaError_t launch_underflow(const void *q, const void *k, int B, int H, int N, 
         underflow_kernel<128><<<grid, kUfRows, 0, stream>>>(qb, kb, counts, H, N, tau, scale, slopes);
     else if (d == 64)
         underflow_kernel<64><<<grid, kUfRows, 0, stream>>>(qb, kb, counts, H, N, tau, scale, slopes);
+    else if (d == 32)
+        underflow_kernel<32><<<grid, kUfRows, 0, stream>>>(qb, kb, counts, H, N, tau, scale, slopes);
+    else if (d == 16)
+        underflow_kernel<16><<<grid, kUfRows, 0, stream>>>(qb, kb, counts, H, N, tau, scale, slopes);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

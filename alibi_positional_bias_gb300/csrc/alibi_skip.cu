@@ -204,6 +204,12 @@ cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, 
     } else if (d == 64) {
         kmax_kernel<64><<<g1, 256, 0, stream>>>(kb, N, kmax2);
         item_plan_kernel<64><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
+    } else if (d == 32) {
+        kmax_kernel<32><<<g1, 256, 0, stream>>>(kb, N, kmax2);
+        item_plan_kernel<32><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
+    } else if (d == 16) {
+        kmax_kernel<16><<<g1, 256, 0, stream>>>(kb, N, kmax2);
+        item_plan_kernel<16><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
     } else {
         return cudaErrorInvalidValue;
     }

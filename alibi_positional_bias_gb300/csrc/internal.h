@@ -37,9 +37,11 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint
 // Decode split plan (alibi_decode.cu): number of KV splits for B*H heads of length L.
 int decode_splits(int BH, int L);
 // Bytes of split-K partials the decode needs for that plan (0 when it does not split).
-size_t decode_partials_bytes(int BH, int splits);
+size_t decode_partials_bytes(int BH, int splits, int d);
+// Head sizes the decode kernels are built for (16, 32, 64, 128).
+bool decode_supports(int d);
 // Launch the decode kernels with a caller-provided partials buffer (used when splits > 1).
-cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L,
+cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
                                const Slopes &slopes, int splits, float *partials, cudaStream_t stream);
 
 // Prefill flags (the values of ALIBI_FWD_* in alibi.h).

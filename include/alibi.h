@@ -72,7 +72,8 @@ ALIBI_API int alibi_slopes(int H, float *out_host);
  * q, k, v: device bf16 [B, H, N, d]; out: device bf16 [B, H, N, d];
  * lse: device fp32 [B, H, N] (may be NULL to skip it);
  * LSE_i = ln sum_{j<=i} exp(q_i.k_j/sqrt(d) - m_h (i - j)).
- * d in {64, 128}; N >= 1; causal = 1 (0: symmetric bias over all keys, see
+ * d in {16, 32, 64, 128} (16 and 32 run the d = 64 tiles with zero columns);
+ * N >= 1; causal = 1 (0: symmetric bias over all keys, see
  * alibi_attn_fwd_ex).
  * Runs the tcgen05/TMEM/TMA kernel: scores and P.V on the tensor cores with
  * fp32 accumulation; the bias is generated from tile coordinates and never
@@ -146,7 +147,7 @@ ALIBI_API int alibi_slopes_explicit(int H, double delta_first, double delta_last
  * first_tile[w] is the first 128-key tile the skipping kernel computes; tiles
  * 0 .. first_tile[w]-1 are left out. first_tile: device int32 [B*H*ceil(N/256)].
  * slopes: optional HOST array of H slopes as in alibi_fwd_options (NULL:
- * alibi_slopes(H)). d in {64, 128}.
+ * alibi_slopes(H)). d in {16, 32, 64, 128}.
  */
 ALIBI_API int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const float *slopes,
                    int *first_tile, void *stream);
@@ -196,7 +197,7 @@ ALIBI_API int alibi_attn_fwd_f32(const float *q, const float *k, const float *v,
  * attending to keys 0..L-1 of the cache ("ALiBi: Attention with Linear
  * Biases", KV-cache paragraph): s_j = q.k_j/sqrt(d) - m_h (L - 1 - j).
  * q: device bf16 [B, H, d]; kcache, vcache: device bf16 [B, H, L, d];
- * out: device bf16 [B, H, d]. d == 128; L >= 1.
+ * out: device bf16 [B, H, d]. d in {16, 32, 64, 128}; L >= 1.
  * Split-K over the cache with an fp32 partial-softmax merge. When it splits,
  * the partials buffer is taken from a library-owned stream-ordered memory pool
  * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).
@@ -253,7 +254,7 @@ ALIBI_API int alibi_attn_probs_f32_ex(const float *q, const float *k, const floa
  * x_ij - M_i (natural-log units, x_ij = q_i.k_j/sqrt(d) - m_h (i - j),
  * M_i = max_j x_ij) is <= tau. Two passes per row in fp32 (row max, then
  * count). q, k: device bf16 [B, H, N, d]; counts: device uint64 [H],
- * overwritten (zeroed on `stream` first). d in {64, 128}.
+ * overwritten (zeroed on `stream` first). d in {16, 32, 64, 128}.
  */
 ALIBI_API int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N, int d, float tau,
                               unsigned long long *counts, void *stream);

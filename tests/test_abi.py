@@ -101,7 +101,7 @@ def test_fwd_argument_errors(lib):
     assert f(P, P, P, P, P, 1, 1, 0, 64, 1, None) == ab.ALIBI_ERR_INVALID
     assert f(MIS, P, P, P, P, 1, 1, 8, 64, 1, None) == ab.ALIBI_ERR_INVALID
     assert f(P, P, P, P, P, 1, 1, 8, 64, 2, None) == ab.ALIBI_ERR_INVALID
-    assert f(P, P, P, P, P, 1, 1, 8, 32, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, 1, 1, 8, 48, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert f(P, P, P, P, P, 1, 300, 8, 64, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
 
 
@@ -116,7 +116,7 @@ def test_fwd_ex_flags_and_plan_errors(lib):
         o, keep = _opt(*opt)
         return lib.alibi_attn_fwd_ex(P, P, P, P, P, 1, H, 8, d, causal, o, None)
     assert f(1, 64, 1, 16) == ab.ALIBI_ERR_INVALID                      # unknown flag
-    assert f(1, 32, 1, 1) == ab.ALIBI_ERR_UNSUPPORTED                   # head size
+    assert f(1, 48, 1, 1) == ab.ALIBI_ERR_UNSUPPORTED                   # head size
     assert f(1, 64, 1, 2, 1.0) == ab.ALIBI_ERR_INVALID                  # clamp >= 0
     assert f(1, 64, 1, 8, 0.0, -5.0) == ab.ALIBI_ERR_INVALID            # z <= 0
     assert f(1, 64, 1, 1 | 4) == ab.ALIBI_ERR_INVALID                   # skip + logdist
@@ -133,7 +133,8 @@ def test_fwd_ex_flags_and_plan_errors(lib):
 def test_decode_and_aux_argument_errors(lib):
     assert lib.alibi_attn_decode(None, P, P, P, 1, 1, 8, 128, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 0, 128, None) == ab.ALIBI_ERR_INVALID
-    assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 8, 64, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 8, 48, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_decode(P, P, P, P, 1, 1, 8, 256, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_fwd_f32(P, P, P, P, P, 1, 1, 8, 512, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_probs_f32(P, P, None, P, 1, 1, 8, 16, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_probs_f32_ex(P, P, P, P, 1, 1, 8, 16, 2, None) == ab.ALIBI_ERR_INVALID

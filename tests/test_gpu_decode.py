@@ -27,6 +27,20 @@ def test_decode_sweep(ab, B, H, L):
     assert_bf16_out(host64(out), ro)
 
 
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("B,H,L", [(1, 3, 5), (2, 2, 129), (1, 4, 1000), (3, 5, 4097), (1, 2, 20000)])
+def test_decode_head_sizes(ab, B, H, L, d):
+    # the smaller head sizes: one key row per d/8 lanes, with and without split-K
+    w = gen.Workload("dec", "decode", B, H, L, d, "bf16", seed=31 + L + d)
+    q, k, v = gen.generate(w)
+    out = ab.alibi_attn_decode(dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16"))
+    out2 = ab.alibi_attn_decode_noalloc(dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16"), out.clone())
+    ab.alibi_check_error()
+    ro, _ = oracle.decode(q.f32, k.f32, v.f32)
+    assert_bf16_out(host64(out), ro)
+    assert np.array_equal(host64(out), host64(out2))
+
+
 def test_decode_matches_prefill_last_row(ab):
     # decode at position L-1 sees what prefill row L-1 sees (same kernel family, same inputs)
     B, H, L = 1, 4, 777

@@ -117,3 +117,25 @@ def test_lazy_rescale_with_divergent_rows(ab):
     ro, rl, _ = oracle.attention(qt.f32, kt.f32, vt.f32)
     assert_bf16_out(out, ro)
     assert_close(lse, rl, TOL_BF16_LSE, "lse")
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("B,H,N,d", [(1, 2, 7, 16), (1, 4, 300, 16), (2, 3, 129, 32), (1, 4, 700, 32)])
+def test_prefill_small_head_sizes(ab, B, H, N, d, causal):
+    # d = 16 and 32 run the d = 64 tiles with a 64-column TMA box over the narrower rows
+    q, k, v = gen.random_case(61 + N + d, B, H, N, d, dtype="bf16")
+    out, lse = ab.alibi_attn_fwd(dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16"), causal=causal)
+    ab.alibi_check_error()
+    ro, rl, _ = oracle.attention(q.f32, k.f32, v.f32, causal=causal)
+    assert_bf16_out(host64(out), ro)
+    assert_close(host64(lse), rl, TOL_BF16_LSE, "lse")
+
+
+def test_prefill_small_head_skip_is_bit_identical(ab):
+    import torch
+    q, k, v = gen.random_case(71, 1, 4, 2000, 32, dtype="bf16")
+    qd, kd, vd = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    o0, l0 = ab.alibi_attn_fwd(qd, kd, vd)
+    o1, l1 = ab.alibi_attn_fwd(qd, kd, vd, skip_underflow=True)
+    ab.alibi_check_error()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
