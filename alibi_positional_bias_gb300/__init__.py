@@ -24,6 +24,7 @@ __all__ = [
     "alibi_attn_fwd", "alibi_attn_fwd_ex", "alibi_attn_skip_plan", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
     "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc", "alibi_selftest_timeout",
     "alibi_slopes_explicit", "alibi_attn_probs_f32_ex", "AlibiFwdOptions", "alibi_attn_bwd", "alibi_attn_bwd_f32",
+    "alibi_kv_block_norms", "alibi_attn_decode_skip",
 ]
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
@@ -74,6 +75,8 @@ def load(build_if_missing: bool = False):
         lib.alibi_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I,
                                         ctypes.POINTER(AlibiFwdOptions), vp]
         lib.alibi_attn_bwd_f32.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, I, vp]
+        lib.alibi_kv_block_norms.argtypes = [vp, vp, I, I, I, I, I, vp]
+        lib.alibi_attn_decode_skip.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, vp]
         lib.alibi_attn_probs_f32_ex.argtypes = [vp, vp, vp, vp, I, I, I, I, I, vp]
         lib.alibi_attn_fwd_ex.restype = I
         lib.alibi_attn_skip_plan.argtypes = [vp, vp, I, I, I, I, ctypes.POINTER(F), vp, vp]
@@ -320,6 +323,38 @@ def alibi_attn_decode(q, kcache, vcache, out=None, stream=None):
     _need(out, torch.bfloat16, (B, H, d), "out")
     _check(load().alibi_attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, L, d,
                                     _stream(stream, q.device)), "alibi_attn_decode")
+    return out
+
+
+def alibi_kv_block_norms(kcache, knorm=None, blk_begin: int = 0, stream=None):
+    """Maximum key norm per 64-key block of a bf16 cache [B, H, L, d] -> fp32 [B, H, ceil(L/64)].
+    Only blocks >= blk_begin are recomputed (refresh the tail after appending keys)."""
+    import torch
+    _need(kcache, torch.bfloat16, None, "kcache")
+    B, H, L, d = kcache.shape
+    nblk = (L + 63) // 64
+    if knorm is None:
+        knorm = torch.empty((B, H, nblk), dtype=torch.float32, device=kcache.device)
+    _need(knorm, torch.float32, (B, H, nblk), "knorm")
+    _check(load().alibi_kv_block_norms(_ptr(kcache), _ptr(knorm), B, H, L, d, int(blk_begin),
+                                       _stream(stream, kcache.device)), "alibi_kv_block_norms")
+    return knorm
+
+
+def alibi_attn_decode_skip(q, kcache, vcache, knorm, out=None, stream=None):
+    """Decode that skips cache rows whose weights are provably below 2^-127 of the
+    largest (needs the cache's block norms from alibi_kv_block_norms)."""
+    import torch
+    _need(kcache, torch.bfloat16, None, "kcache")
+    B, H, L, d = kcache.shape
+    _need(vcache, torch.bfloat16, kcache.shape, "vcache")
+    _need(q, torch.bfloat16, (B, H, d), "q")
+    _need(knorm, torch.float32, (B, H, (L + 63) // 64), "knorm")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, (B, H, d), "out")
+    _check(load().alibi_attn_decode_skip(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(knorm), _ptr(out), B, H, L, d,
+                                         _stream(stream, q.device)), "alibi_attn_decode_skip")
     return out
 
 

@@ -16,6 +16,15 @@
 // merges its warps' partial softmaxes in shared memory, and either writes the
 // output (one split) or an fp32 partial (m, l, o[d]) that a second kernel
 // merges.
+//
+// Skipping ("When Attention Goes Blind" sec. 3.2-3.3 and 5.2: past its blindness
+// distance a head's weights are exactly zero): with per-64-key-block maximum key
+// norms (kv_block_norms_kernel, kept by the caller alongside the cache), a warp
+// step is left out when every key j in it satisfies, in base-2 units,
+//   c1 |q| max|k| - m log2(e) (L - 1 - j) <= x_last - 127
+// where x_last is the last key's logit, a lower bound of the final row max:
+// each such weight is below 2^-127 of the largest one, i.e. below the fp32
+// resolution of the sum, and its K and V rows are never read.
 
 #include "ptx.cuh"
 
@@ -37,7 +46,8 @@ struct DecodeParams {
     const __nv_bfloat16 *q, *k, *v;
     __nv_bfloat16 *out;
     float *part;  // [BH][splits][kPartStride], used when splits > 1
-    int H, L, splits, chunk;
+    const float *knorm;  // optional [BH][nblk] max key norm per 64-key block: enables skipping
+    int H, L, splits, chunk, nblk;
     float c1;  // log2(e) / sqrt(d)
     Slopes slopes;
 };
@@ -91,7 +101,44 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
 #pragma unroll
     for (int t = 0; t < 8; ++t) o[t] = 0.f;
 
-    for (int blk = kbeg + warp * C::kKeysPerWarp; blk < kend; blk += kWarps * C::kKeysPerWarp) {
+    // Skip set-up: |q| c1 and the last key's logit (both the same in every lane group).
+    const bool skip = p.knorm != nullptr;
+    float skip_a = 0.f;  // c1 |q| (1 + 2^-10)^2: multiplies a block's max key norm
+    float skip_b = 0.f;  // -x_last + |x_last| 2^-10 + 127: with the above, the bias a step must exceed
+    const float *kn = skip ? p.knorm + static_cast<size_t>(bh) * p.nblk : nullptr;
+    if (skip) {
+        float ss = 0.f, dl = 0.f;
+        float kf[8];
+        bf16x8_to_f32(ld_stream(kbase + static_cast<size_t>(pos) * D), kf);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            ss = fmaf(qf[t], qf[t], ss);
+            dl = fmaf(qf[t], kf[t], dl);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off; off >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            dl += __shfl_xor_sync(0xffffffffu, dl, off);
+        }
+        const float slack = 1.0f + 0x1p-10f;
+        skip_a = sqrtf(ss) * slack * slack;
+        skip_b = -dl + fabsf(dl) * 0x1p-10f + 127.0f;
+    }
+    // max key norm over the norm blocks a warp step [b, b + KPW) touches
+    auto step_norm = [&](int b) -> float {
+        const int b0 = b >> 6, b1 = min((b + C::kKeysPerWarp - 1) >> 6, p.nblk - 1);
+        return fmaxf(__ldg(kn + b0), __ldg(kn + b1));
+    };
+    const int first = kbeg + warp * C::kKeysPerWarp, stride = kWarps * C::kKeysPerWarp;
+    float kn_cur = (skip && first < kend) ? step_norm(first) : 0.f;
+
+    for (int blk = first; blk < kend; blk += stride) {
+        // next step's norm fetched one step ahead, off the load path
+        const float kn_nxt = (skip && blk + stride < kend) ? step_norm(blk + stride) : 0.f;
+        const bool drop = skip && sl2 * static_cast<float>(pos - min(blk + C::kKeysPerWarp - 1, kend - 1)) >=
+                                      fmaf(skip_a, kn_cur, skip_b);
+        kn_cur = kn_nxt;
+        if (drop) continue;  // every weight of this step is below 2^-127 of the row's largest
         uint4 kr[kKeysPerGroup], vr[kKeysPerGroup];
 #pragma unroll
         for (int u = 0; u < kKeysPerGroup; ++u) {
@@ -223,7 +270,64 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restri
     *reinterpret_cast<uint2 *>(out + static_cast<size_t>(warp) * D + 4 * lane) = pk;
 }
 
+// Maximum key norm of each 64-key block of the cache: grid (blocks, B*H), 256
+// threads, d/8 lanes per key. Blocks [blk_begin, nblk) of every (b, h).
+template <int D>
+__global__ void __launch_bounds__(256) kv_block_norms_kernel(const __nv_bfloat16 *__restrict__ k, float *__restrict__ knorm,
+                                                             int L, int nblk, int blk_begin)
+{
+    constexpr int LPR = D / 8, RPW = 32 / LPR;
+    __shared__ float red[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blk_begin + blockIdx.x, bh = blockIdx.y;
+    const int g = lane / LPR, l = lane % LPR;
+    const __nv_bfloat16 *kb = k + static_cast<size_t>(bh) * L * D + 8 * l;
+    float best = 0.f;
+    // uniform trip count: every lane takes part in the shuffles
+    for (int j0 = b * 64 + warp * RPW; j0 < b * 64 + 64; j0 += 8 * RPW) {
+        const int j = j0 + g;
+        float ss = 0.f;
+        if (j < L) {
+            float kf[8];
+            bf16x8_to_f32(ld_stream(kb + static_cast<size_t>(j) * D), kf);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) ss = fmaf(kf[t], kf[t], ss);
+        }
+        // the row's sum of squares over its d/8 lanes
+#pragma unroll
+        for (int off = LPR / 2; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        best = fmaxf(best, ss);
+    }
+    // max over the rows this warp saw
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, off));
+    if (lane == 0) red[warp] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float mx = red[0];
+        for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
+        knorm[static_cast<size_t>(bh) * nblk + b] = sqrtf(mx);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, int L, int d, int blk_begin,
+                                  cudaStream_t stream)
+{
+    const int nblk = (L + 63) / 64;
+    if (blk_begin >= nblk) return cudaSuccess;
+    dim3 grid(nblk - blk_begin, B * H);
+    const auto *k = static_cast<const __nv_bfloat16 *>(kc);
+    switch (d) {
+        case 128: kv_block_norms_kernel<128><<<grid, 256, 0, stream>>>(k, knorm, L, nblk, blk_begin); break;
+        case 64: kv_block_norms_kernel<64><<<grid, 256, 0, stream>>>(k, knorm, L, nblk, blk_begin); break;
+        case 32: kv_block_norms_kernel<32><<<grid, 256, 0, stream>>>(k, knorm, L, nblk, blk_begin); break;
+        case 16: kv_block_norms_kernel<16><<<grid, 256, 0, stream>>>(k, knorm, L, nblk, blk_begin); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
 
 // Split count: enough CTAs for several waves (two resident per SM), at least
 // 512 keys per split, and every split non-empty.
@@ -245,8 +349,8 @@ size_t decode_partials_bytes(int BH, int splits, int d)
 bool decode_supports(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 template <int D>
-static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L,
-                                   const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
+static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B,
+                                   int H, int L, const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
 {
     using C = DecCfg<D>;
     DecodeParams p;
@@ -263,6 +367,8 @@ static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc
     p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     p.slopes = slopes;
     const int BH = B * H;
+    p.knorm = knorm;
+    p.nblk = (L + 63) / 64;
     // recompute splits so that no split is empty after rounding the chunk
     p.splits = (L + p.chunk - 1) / p.chunk;
     if (p.splits > splits) return cudaErrorInvalidValue;
@@ -274,29 +380,30 @@ static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
-                               const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
+cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B,
+                               int H, int L, int d, const Slopes &slopes, int splits, float *partials,
+                               cudaStream_t stream)
 {
     switch (d) {
-        case 128: return launch_decode_d<128>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
-        case 64: return launch_decode_d<64>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
-        case 32: return launch_decode_d<32>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
-        case 16: return launch_decode_d<16>(q, kc, vc, out, B, H, L, slopes, splits, partials, stream);
+        case 128: return launch_decode_d<128>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
+        case 64: return launch_decode_d<64>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
+        case 32: return launch_decode_d<32>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
+        case 16: return launch_decode_d<16>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
-                          const Slopes &slopes, cudaStream_t stream)
+cudaError_t launch_decode(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B, int H,
+                          int L, int d, const Slopes &slopes, cudaStream_t stream)
 {
     if (!decode_supports(d)) return cudaErrorInvalidValue;
     const int BH = B * H;
     const int splits = decode_splits(BH, L);
-    if (splits == 1) return launch_decode_with(q, kc, vc, out, B, H, L, d, slopes, 1, nullptr, stream);
+    if (splits == 1) return launch_decode_with(q, kc, vc, knorm, out, B, H, L, d, slopes, 1, nullptr, stream);
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, decode_partials_bytes(BH, splits, d), decode_pool(), stream);
     if (e != cudaSuccess) return e;
-    e = launch_decode_with(q, kc, vc, out, B, H, L, d, slopes, splits, static_cast<float *>(ws), stream);
+    e = launch_decode_with(q, kc, vc, knorm, out, B, H, L, d, slopes, splits, static_cast<float *>(ws), stream);
     cudaError_t f = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : f;
 }

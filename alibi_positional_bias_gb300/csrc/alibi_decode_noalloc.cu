@@ -72,7 +72,7 @@ extern "C" int alibi_attn_decode_noalloc(const void *q, const void *kcache, cons
     fill_slopes(H, &s);
     // Every partial the merge reads is written earlier in the same call, so the
     // buffer needs no clearing; what the previous call left there is overwritten.
-    const cudaError_t e = launch_decode_with(q, kcache, vcache, out, B, H, L, d, s, splits,
+    const cudaError_t e = launch_decode_with(q, kcache, vcache, nullptr, out, B, H, L, d, s, splits,
                                              splits > 1 ? scratch : nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ALIBI_OK : ALIBI_ERR_CUDA;
 }

@@ -364,7 +364,33 @@ int alibi_attn_decode(const void *q, const void *kcache, const void *vcache, voi
     if (!decode_supports(d)) return ALIBI_ERR_UNSUPPORTED;
     Slopes s;
     fill_slopes(H, &s);
-    return to_status(launch_decode(q, kcache, vcache, out, B, H, L, d, s, static_cast<cudaStream_t>(stream)));
+    return to_status(launch_decode(q, kcache, vcache, nullptr, out, B, H, L, d, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_kv_block_norms(const void *kcache, float *knorm, int B, int H, int L, int d, int blk_begin, void *stream)
+{
+    if (!kcache || !knorm) return ALIBI_ERR_INVALID;
+    if (!aligned16(kcache) || (reinterpret_cast<uintptr_t>(knorm) & 3u)) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, L, d);
+    if (st != ALIBI_OK) return st;
+    if (!decode_supports(d)) return ALIBI_ERR_UNSUPPORTED;
+    if (blk_begin < 0 || blk_begin > (L + 63) / 64) return ALIBI_ERR_INVALID;
+    return to_status(launch_kv_block_norms(kcache, knorm, B, H, L, d, blk_begin, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_attn_decode_skip(const void *q, const void *kcache, const void *vcache, const float *knorm, void *out, int B,
+                           int H, int L, int d, void *stream)
+{
+    if (!q || !kcache || !vcache || !knorm || !out) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(knorm) & 3u))
+        return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, L, d);
+    if (st != ALIBI_OK) return st;
+    if (!decode_supports(d)) return ALIBI_ERR_UNSUPPORTED;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_decode(q, kcache, vcache, knorm, out, B, H, L, d, s, static_cast<cudaStream_t>(stream)));
 }
 
 int alibi_attn_decode_splits(int B, int H, int L, int d)

@@ -41,8 +41,12 @@ size_t decode_partials_bytes(int BH, int splits, int d);
 // Head sizes the decode kernels are built for (16, 32, 64, 128).
 bool decode_supports(int d);
 // Launch the decode kernels with a caller-provided partials buffer (used when splits > 1).
-cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
-                               const Slopes &slopes, int splits, float *partials, cudaStream_t stream);
+cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B,
+                               int H, int L, int d, const Slopes &slopes, int splits, float *partials,
+                               cudaStream_t stream);
+// Maximum key norm per 64-key block, blocks [blk_begin, ceil(L/64)) of every (b, h).
+cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, int L, int d, int blk_begin,
+                                  cudaStream_t stream);
 
 // Prefill flags (the values of ALIBI_FWD_* in alibi.h).
 constexpr unsigned int kFwdSkipUnderflow = 1u;
@@ -64,8 +68,8 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
                            int H, int N, int d, int causal, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N,
                              int d, int causal, const Slopes &slopes, cudaStream_t stream);
-cudaError_t launch_decode(const void *q, const void *kc, const void *vc, void *out, int B, int H, int L, int d,
-                          const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_decode(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B, int H,
+                          int L, int d, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_bwd_tc(const void *q, const void *k, const void *v, const void *out, const float *lse,
                           const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d, int causal,
                           unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,

@@ -441,6 +441,32 @@ def run_native(args):
                             "frac": tf / peaks["bf16_tflops"]}
             del to, oo, lo
 
+    # -------------------- decode skipping provably underflowed cache rows (block key norms kept with
+    # the cache; computed once here, outside the timed loop, as a serving loop would keep them)
+    dskip = None
+    if do_dec:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        knorm = ab.alibi_kv_block_norms(dk, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        norm_ms = ev0.elapsed_time(ev1)
+        t_ds = timed_ms(lambda: ab.alibi_attn_decode_skip(dq, dk, dv, knorm, out=dout, stream=stream))
+        # share of cache rows left out, by the kernel's own rule at 64-key granularity (reporting only)
+        with torch.no_grad():
+            c1 = 1.4426950408889634 / wd.d ** 0.5
+            qf = dq.float() * c1
+            qn = qf.norm(dim=-1) * (1 + 2.0 ** -10) ** 2
+            xl = (qf * dk[:, :, -1].float()).sum(-1)
+            sl2 = torch.tensor(ab.alibi_slopes(wd.H) * 1.4426950408889634, device=dev).view(1, -1, 1)
+            nb = knorm.shape[2]
+            jl = torch.clamp(torch.arange(nb, device=dev) * 64 + 63, max=wd.N - 1).view(1, 1, -1).float()
+            thr = qn[..., None] * knorm - xl[..., None] + xl.abs()[..., None] * 2.0 ** -10 + 127.0
+            skipped = (sl2 * (wd.N - 1 - jl) >= thr).float().mean().item()
+        dskip = {"ms": t_ds, "effective_gbs": world * decode_bytes(wd) / (t_ds / 1e3) / 1e9, "unit": "GB/s",
+                 "rows_skipped_frac": skipped, "block_norms_ms_once": norm_ms,
+                 "exact": "omitted weights < 2^-127 of the largest; matches the dense decode to bf16 rounding (tested)"}
+
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
     e2e_dec = None
@@ -561,6 +587,7 @@ def run_native(args):
         "prefill_steep_slopes": steep,
         "backward": backward,
         "prefill_other_configs": others,
+        "decode_skip_underflow": dskip,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,

@@ -206,6 +206,32 @@ ALIBI_API int alibi_attn_decode(const void *q, const void *kcache, const void *v
                       int B, int H, int L, int d, void *stream);
 
 /*
+ * Per-block maximum key norms for skipping in the decode: knorm[b][h][c] =
+ * max over keys j in [64 c, 64 c + 64) of |k_j|_2 (fp32, from the bf16 cache).
+ * kcache: device bf16 [B, H, L, d]; knorm: device fp32 [B, H, ceil(L/64)],
+ * caller-owned. Only blocks c >= blk_begin are (re)computed, so a serving loop
+ * that appends keys refreshes the tail block(s) alone (blk_begin = old L / 64);
+ * blk_begin = 0 computes all. d in {16, 32, 64, 128}.
+ */
+ALIBI_API int alibi_kv_block_norms(const void *kcache, float *knorm, int B, int H, int L, int d, int blk_begin,
+                   void *stream);
+
+/*
+ * alibi_attn_decode that leaves out the cache rows whose weights are provably
+ * below 2^-127 of the row's largest ("When Attention Goes Blind" sec. 3.2-3.3
+ * and 5.2: past a head's blindness distance its weights underflow; steep heads
+ * act as sliding windows). With the last key's logit x_last as a lower bound of
+ * the row max and c1 = log2(e)/sqrt(d), a step of keys is skipped when
+ * c1 |q| max|k| - m_h log2(e) (L - 1 - j) <= x_last - 127 for all its keys
+ * (with a 2^-10 relative slack on the norms); those K and V rows are never
+ * read. The omitted weights are below the fp32 resolution of the normaliser, so
+ * the output matches alibi_attn_decode within rounding. knorm from
+ * alibi_kv_block_norms for the same cache. Other arguments as alibi_attn_decode.
+ */
+ALIBI_API int alibi_attn_decode_skip(const void *q, const void *kcache, const void *vcache, const float *knorm,
+                   void *out, int B, int H, int L, int d, void *stream);
+
+/*
  * Number of KV-cache splits alibi_attn_decode uses for this shape (host-only,
  * deterministic for a given device). 1 means a single kernel with no partials
  * buffer; S > 1 means a split kernel plus a merge kernel and a partials buffer

@@ -177,3 +177,13 @@ def test_bwd_argument_errors(lib):
     assert f(P, P, P, P, P, P, P, P, P, 1, 1, 8, 64, 1, o, None) == ab.ALIBI_ERR_INVALID
     assert lib.alibi_attn_bwd_f32(P, P, P, P, P, P, P, P, P, 1, 1, 8, 300, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_bwd_f32(P, P, P, None, P, P, P, P, P, 1, 1, 8, 16, 1, None) == ab.ALIBI_ERR_INVALID
+
+
+def test_decode_skip_argument_errors(lib):
+    assert lib.alibi_kv_block_norms(None, P, 1, 1, 8, 128, 0, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_kv_block_norms(P, P, 1, 1, 8, 128, 2, None) == ab.ALIBI_ERR_INVALID     # blk_begin > ceil(L/64)
+    assert lib.alibi_kv_block_norms(P, P, 1, 1, 8, 128, -1, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_kv_block_norms(P, P, 1, 1, 8, 48, 0, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_decode_skip(P, P, P, None, P, 1, 1, 8, 128, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_decode_skip(P, P, P, P, MIS, 1, 1, 8, 128, None) == ab.ALIBI_ERR_INVALID
+    assert lib.alibi_attn_decode_skip(P, P, P, P, P, 1, 1, 8, 96, None) == ab.ALIBI_ERR_UNSUPPORTED
