@@ -593,10 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_after();
             const float inv_l = 1.0f / l;
             const bool valid = i < p.N;
-            __nv_bfloat16 *orow = p.out + (static_cast<size_t>(t.bh) * p.N + (valid ? i : 0)) * p.dr;
+            // only the D = 64 kernel serves smaller head sizes; D = 128 keeps a compile-time row size
+            const int dr = D == 64 ? p.dr : D;
+            __nv_bfloat16 *orow = p.out + (static_cast<size_t>(t.bh) * p.N + (valid ? i : 0)) * dr;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                if (c * 32 >= p.dr) break;  // columns past a smaller head size are zero and not stored
+                if (c * 32 >= dr) break;  // columns past a smaller head size are zero and not stored
                 uint32_t o[32];
                 tmem_ld32(lane_addr + 256 + s * 128 + c * 32, o);
                 tmem_wait_ld();
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv_l, __uint_as_float(o[2 * u + 1]) * inv_l);
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                    const int n16 = min(4, (p.dr - c * 32) / 8);  // 16-byte stores in this chunk
+                    const int n16 = min(4, (dr - c * 32) / 8);  // 16-byte stores in this chunk
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         if (u < n16) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
