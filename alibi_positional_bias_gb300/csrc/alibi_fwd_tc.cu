@@ -62,11 +62,14 @@ struct Cfg {
     static constexpr uint32_t kQ = 0;                      // 2 Q tiles
     static constexpr uint32_t kK = 2 * kTileBytes;         // K ring
     static constexpr uint32_t kV = kK + kKStages * kTileBytes;  // V ring
-    // One 128 x 64 swizzle atom of bias operands for the causal kernel: K-step 0
-    // holds ones (A side), K-steps 1 and 2 the per-head column bias of two items
-    // in flight (B side).
+    // Two 128 x 64 swizzle atoms of bias operands: atom A holds ones (K-step 0, the
+    // A side), the column bias of keys before the rows, +m log2(e) c / c1, for the
+    // two items in flight (K-steps 1, 2), and that of keys after the rows,
+    // -m log2(e) c / c1 (non-causal), for item parity 0 (K-step 3); atom B holds
+    // the latter for parity 1 (K-step 0).
     static constexpr uint32_t kAux = kV + kVStages * kTileBytes;
-    static constexpr uint32_t kBar = kAux + kChunkBytes;
+    static constexpr uint32_t kAux2 = kAux + kChunkBytes;
+    static constexpr uint32_t kBar = kAux2 + kChunkBytes;
     static constexpr uint32_t kSmem = kBar + 256 + 1024;   // barriers, TMEM slot, alignment slack
 };
 
@@ -116,11 +119,13 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
-// The causal plain kernel adds the column part of the bias, m log2(e) (k - k0),
-// on the tensor core (the bias operands of ptx.cuh; B row c = m log2(e) c / c1),
-// so S' = q.k + bias / c1 comes out of the accumulator and the softmax only adds
-// the row part nb.
-__device__ __forceinline__ bool use_aux_bias(const FwdParams &p, bool var) { return p.causal && !var; }
+// The plain kernel adds the column part of the bias on the tensor core (the bias
+// operands of ptx.cuh): for a KV tile left of a Q tile's diagonal the bias is
+// -m (i - k0) + m c and B row c holds m log2(e) c / c1; right of it (non-causal)
+// it is -m (k0 - i) - m c and B row c holds -m log2(e) c / c1. S' = q.k + bias / c1
+// comes out of the accumulator and the softmax only adds the row part. Diagonal
+// tiles of the non-causal kernel (|i - k| is not linear in c) take no bias step.
+__device__ __forceinline__ bool use_aux_bias(const FwdParams &p, bool var) { return !var; }
 
 __device__ __forceinline__ float max3f(float a, float b, float c)
 {
@@ -153,7 +158,7 @@ __device__ __forceinline__ int item_index(int k)
 // longest-first: round r holds the 256-row block NQB-1-r of every (b, h). With a
 // plan (underflow skipping), the plan gives the item and the first KV tile worth
 // computing, already sorted by the tiles the item spans.
-__device__ __forceinline__ Item decode_item(const FwdParams &p, int idx)
+__device__ __forceinline__ Item decode_item(const FwdParams &p, int idx, bool causal)
 {
     Item it;
     int first = 0;
@@ -170,7 +175,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int idx)
     const int qt1 = 2 * it.qb + 1;
     it.q1valid = qt1 < p.NQT;
     it.top = it.q1valid ? qt1 : qt1 - 1;
-    it.n = p.causal ? it.top + 1 - first : p.NQT;
+    it.n = causal ? it.top + 1 - first : p.NQT;
     return it;
 }
 
@@ -183,14 +188,14 @@ __device__ __forceinline__ int kv_tile(const FwdParams &p, const Item &t, int it
 
 // Is Q slot s active at iteration `it`? Causal: slot 0 skips the first tile (the
 // diagonal of slot 1 lies entirely above slot 0's rows). Non-causal: always.
-__device__ __forceinline__ bool slot_active(const FwdParams &p, const Item &t, int s, int it)
+__device__ __forceinline__ bool slot_active(const Item &t, int s, int it, bool causal)
 {
-    return s == 1 ? t.q1valid : (t.q1valid && p.causal ? it >= 1 : true);
+    return s == 1 ? t.q1valid : (t.q1valid && causal ? it >= 1 : true);
 }
 
 // VAR: compiled with the sec. 3.4 mitigation path (p.variant selects which ones);
 // the plain ALiBi kernel (VAR = false) carries none of that code.
-template <int D, bool VAR>
+template <int D, bool VAR, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p)
 {
     using C = Cfg<D>;
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
-                const Item t = decode_item(p, w);
+                const Item t = decode_item(p, w, CAUSAL);
                 ok = mbar_wait(q_empty, (k & 1) ^ 1, err, SITE_PROD_Q);
                 if (!ok) break;
                 for (int s = 0; s < 2; ++s) {
@@ -304,13 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t sV = smem_u32(smem + C::kV);
             const bool aux = use_aux_bias(p, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
+            const uint64_t auxd2 = smem_desc_sw128(smem_u32(smem + C::kAux2), 16, 1024);
             uint32_t kc = 0, vc = 0;
             uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
-                const Item t = decode_item(p, w);
+                const Item t = decode_item(p, w, CAUSAL);
                 const int last_slot = t.q1valid ? 1 : 0;
                 ok = mbar_wait(&q_full[0], k & 1, err, SITE_MMA_Q) && mbar_wait(&q_full[1], k & 1, err, SITE_MMA_Q);
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_MMA_Q);
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // swizzle atom, 16 KB per 64-column atom). Descriptors are built once per tile;
                 // each step adds a compile-time offset to the 14-bit address field (smem
                 // addresses stay below 256 KB, so the field never carries).
-                auto issue_S = [&](int s, uint32_t kst) {
+                auto issue_S = [&](int s, uint32_t kst, int jt) {
                     const uint64_t qd = smem_desc_sw128(sQ + s * C::kTileBytes, 16, 1024);
                     const uint64_t kd = smem_desc_sw128(sK + kst * C::kTileBytes, 16, 1024);
                     const uint32_t dst = tmem + s * 128;
@@ -330,8 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         const uint32_t step = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
                         mma_ss_w(dst, qd + step, kd + step, idS, kk > 0);
                     }
-                    // column bias: ones (K-step 0 of the aux atom) x this item's bias rows (K-step 1 + buf)
-                    if (aux) mma_ss_w(dst, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
+                    // column bias: ones (K-step 0 of atom A) x this item's bias rows
+                    if (aux) {
+                        const int qt = 2 * t.qb + s;
+                        if (CAUSAL || jt < qt)
+                            mma_ss_w(dst, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
+                        else if (jt > qt)
+                            mma_ss_w(dst, auxd, (k & 1) ? auxd2 : auxd + 6, idS, 1u);
+                    }
                     mma_commit_w(&s_full[s]);
                 };
                 // O_s += P_s V over the 128 keys in steps of 16 (V is MN-major: d contiguous;
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     for (int s = 0; s < 2; ++s)
-                        if (slot_active(p, t, s, 0)) issue_S(s, st);
+                        if (slot_active(t, s, 0, CAUSAL)) issue_S(s, st, kv_tile(p, t, 0));
                     mma_commit_w(&k_empty[st]);
                 }
                 for (int it = 0; it < t.n && ok; ++it) {
@@ -372,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (!ok) break;
                     }
                     for (int s = 0; s < 2 && ok; ++s) {
-                        if (slot_active(p, t, s, it)) {
+                        if (slot_active(t, s, it, CAUSAL)) {
                             ok = mbar_wait(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
                             if (ok && first_pv[s]) ok = mbar_wait(&o_empty[s], (o_cnt[s] & 1) ^ 1, err, SITE_MMA_O);
                             ok = __all_sync(0xffffffffu, ok);
@@ -391,9 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 ++o_cnt[s];
                             }
                         }
-                        if (it + 1 < t.n && slot_active(p, t, s, it + 1)) {
+                        if (it + 1 < t.n && slot_active(t, s, it + 1, CAUSAL)) {
                             const uint32_t kst = (kc + it + 1) % 2;
-                            issue_S(s, kst);
+                            issue_S(s, kst, kv_tile(p, t, it + 1));
                             if (s == last_slot) mma_commit_w(&k_empty[kst]);
                         }
                     }
@@ -420,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         for (int k = 0; ok; ++k) {
             const int w = item_index(k);
             if (w >= p.num_items) break;
-            const Item t = decode_item(p, w);
+            const Item t = decode_item(p, w, CAUSAL);
             if (s == 0 && use_aux_bias(p, VAR)) {
                 // Column-bias operand, one row per thread, one item ahead: item 0's at the
                 // start, item k+1's at the start of item k (buffer (k+1) & 1; every MMA that
@@ -428,8 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 auto publish = [&](int kk) {
                     const int wn = item_index(kk);
                     if (wn >= p.num_items) return;
-                    const Item tn = decode_item(p, wn);
-                    write_bias_row(smem + C::kAux, r, kk & 1, p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1);
+                    const Item tn = decode_item(p, wn, CAUSAL);
+                    const float bv = p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1;
+                    write_bias_row(smem + C::kAux, r, kk & 1, bv);  // keys before the rows
+                    if (!CAUSAL) {  // keys after the rows
+                        if (kk & 1)
+                            write_bias_pair(smem + C::kAux2, r, 0, -bv);
+                        else
+                            write_bias_pair(smem + C::kAux, r, 3, -bv);
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bias_full[kk & 1]);
@@ -441,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const int qt = 2 * t.qb + s;
             const int i = qt * BM + r;
             const float sl2 = p.slopes.log2e[t.bh % p.H];
-            const int it0 = (s == 0 && t.q1valid && p.causal) ? 1 : 0;
+            const int it0 = (s == 0 && t.q1valid && CAUSAL) ? 1 : 0;
             float M = -INFINITY, l = 0.f;
             for (int it = it0; it < t.n; ++it) {
                 const int j = kv_tile(p, t, it);
@@ -462,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 const float2 c1v = make_float2(p.c1, p.c1);
                 // Non-causal tiles at or right of the diagonal hold keys past the query:
                 // there the distance is |i - k| and the bias -|nb + sl2 c| (sl2 >= 0).
-                const bool sym = !p.causal && j >= qt;
+                const bool sym = !CAUSAL && j >= qt;
                 float x[BN];
                 if (VAR) {
                     // Mitigation variants, element by element in base-2 units:
@@ -489,27 +508,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (clamp) b = fmaxf(b, p.clamp2);
                         x[c] = a + b;
                     }
-                } else if (p.causal) {
-                    // the column part of the bias is already in S (see use_aux_bias)
-                    const float2 nbv = make_float2(nb, nb);
+                } else if (CAUSAL || j != qt) {
+                    // The column part of the bias is already in S (see use_aux_bias); the row
+                    // part is nb for keys before the rows and -nb for keys after them.
+                    const float rb = (CAUSAL || j < qt) ? nb : -nb;
+                    const float2 rbv = make_float2(rb, rb);
 #pragma unroll
                     for (int u = 0; u < BN / 2; ++u) {
                         const float2 xv = __ffma2_rn(
-                            make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, nbv);
-                        x[2 * u] = xv.x;
-                        x[2 * u + 1] = xv.y;
-                    }
-                } else if (!sym) {
-#pragma unroll
-                    for (int u = 0; u < BN / 2; ++u) {
-                        const float2 b = make_float2(fmaf(sl2, static_cast<float>(2 * u), nb),
-                                                     fmaf(sl2, static_cast<float>(2 * u + 1), nb));
-                        const float2 xv = __ffma2_rn(
-                            make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, b);
+                            make_float2(__uint_as_float(sraw[2 * u]), __uint_as_float(sraw[2 * u + 1])), c1v, rbv);
                         x[2 * u] = xv.x;
                         x[2 * u + 1] = xv.y;
                     }
                 } else {
+                    // non-causal diagonal tile (raw S): bias -|nb + sl2 c|
 #pragma unroll
                     for (int u = 0; u < BN / 2; ++u) {
                         const float2 b = make_float2(-fabsf(fmaf(sl2, static_cast<float>(2 * u), nb)),
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         x[2 * u + 1] = xv.y;
                     }
                 }
-                if (p.causal) {
+                if (CAUSAL) {
                     if (j == qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
                         for (int c = 0; c < BN; ++c) x[c] = (c > r) ? -INFINITY : x[c];
@@ -672,15 +684,21 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
         // kLaunchRegs per thread; refuse to launch otherwise (an unbalanced
         // setmaxnreg.inc would wait for registers that never come).
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, VAR>);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(fwd_tc_kernel<D, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
+        for (int c = 0; c < 2; ++c) {
+            const auto kern = c ? fwd_tc_kernel<D, VAR, true> : fwd_tc_kernel<D, VAR, false>;
+            cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
-    fwd_tc_kernel<D, VAR><<<grid, kThreads, C::kSmem, stream>>>(p);
+    if (causal)
+        fwd_tc_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
+    else
+        fwd_tc_kernel<D, VAR, false><<<grid, kThreads, C::kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 

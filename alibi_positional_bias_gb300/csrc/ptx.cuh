@@ -295,8 +295,9 @@ __device__ __forceinline__ void write_ones_chunk(uint8_t *aux, int r, int j)
     *reinterpret_cast<uint4 *>(aux + r * 128 + ((j ^ (r & 7)) << 4)) = v;
 }
 
-// Row r of bias buffer `buf`: the value b as hi + mid + lo bf16 terms.
-__device__ __forceinline__ void write_bias_row(uint8_t *aux, int r, int buf, float b)
+// Row r of the K-step `pair` (logical chunks 2 pair, 2 pair + 1) of an atom: the
+// value b as hi + mid + lo bf16 terms.
+__device__ __forceinline__ void write_bias_pair(uint8_t *atom, int r, int pair, float b)
 {
     const __nv_bfloat16 hi = __float2bfloat16_rn(b);
     const float r1 = b - __bfloat162float(hi);
@@ -305,10 +306,16 @@ __device__ __forceinline__ void write_bias_row(uint8_t *aux, int r, int buf, flo
     const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
                         (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
     const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
-    const int j0 = 2 + 2 * buf;
-    uint8_t *row = aux + r * 128;
+    const int j0 = 2 * pair;
+    uint8_t *row = atom + r * 128;
     *reinterpret_cast<uint4 *>(row + ((j0 ^ (r & 7)) << 4)) = make_uint4(w0, w1, 0u, 0u);
     *reinterpret_cast<uint4 *>(row + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Row r of bias buffer `buf` (K-step 1 + buf of the atom that holds the ones).
+__device__ __forceinline__ void write_bias_row(uint8_t *aux, int r, int buf, float b)
+{
+    write_bias_pair(aux, r, 1 + buf, b);
 }
 
 // ---------------------------------------------------------------- numerics
