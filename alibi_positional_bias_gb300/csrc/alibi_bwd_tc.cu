@@ -118,7 +118,7 @@ __device__ __forceinline__ float var_weight(const BwdParams &p, float mnat, floa
 // Causal plain kernels add the column part of the bias on the tensor core (the bias
 // operands of ptx.cuh): one more K-step after S = Q K^T (dQ; B row = key column c:
 // m log2(e) c / c1) or S^T = K Q^T (dK/dV; B row = query column c: -m log2(e) c / c1).
-__device__ __forceinline__ bool bwd_aux(const BwdParams &p, bool var) { return p.causal && !var; }
+__device__ __forceinline__ bool bwd_aux(bool causal, bool var) { return causal && !var; }
 
 enum : uint32_t {
     SITE_B_PROD_RES = 0x401, SITE_B_PROD_RING = 0x402, SITE_B_MMA_RES = 0x411, SITE_B_MMA_RING = 0x412,
@@ -138,30 +138,30 @@ struct BItem {
 
 // dKdV items: round r of the schedule is KV tile r of every (b, h) (causal: the
 // longest first, since tile jt meets NT - jt query tiles).
-__device__ __forceinline__ BItem dkdv_item(const BwdParams &p, int idx)
+__device__ __forceinline__ BItem dkdv_item(const BwdParams &p, int idx, bool causal)
 {
     BItem it;
     const int round = idx / p.BH;
     it.bh = idx - round * p.BH;
     it.tile = round;
-    it.n = p.causal ? p.NT - round : p.NT;
+    it.n = causal ? p.NT - round : p.NT;
     return it;
 }
 
 // Query tile visited at iteration `it` of a dKdV item (causal: from the diagonal up).
-__device__ __forceinline__ int dkdv_qtile(const BwdParams &p, const BItem &t, int it)
+__device__ __forceinline__ int dkdv_qtile(const BItem &t, int it, bool causal)
 {
-    return p.causal ? t.tile + it : it;
+    return causal ? t.tile + it : it;
 }
 
 // dQ items: round r is query tile NT - 1 - r of every (b, h) (causal: longest first).
-__device__ __forceinline__ BItem dq_item(const BwdParams &p, int idx)
+__device__ __forceinline__ BItem dq_item(const BwdParams &p, int idx, bool causal)
 {
     BItem it;
     const int round = idx / p.BH;
     it.bh = idx - round * p.BH;
     it.tile = p.NT - 1 - round;
-    it.n = p.causal ? it.tile + 1 : p.NT;
+    it.n = causal ? it.tile + 1 : p.NT;
     return it;
 }
 
@@ -211,7 +211,7 @@ __device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0
 
 // ------------------------------------------------------------------ dK, dV
 
-template <int D, bool VAR>
+template <int D, bool VAR, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p)
 {
     using C = BwdCfg<D>;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (bwd_aux(p, VAR) && threadIdx.x < 2 * BT) {
+    if (bwd_aux(CAUSAL, VAR) && threadIdx.x < 2 * BT) {
         write_ones_chunk(smem + C::kAux, threadIdx.x >> 1, threadIdx.x & 1);
         fence_proxy_async_smem();
     }
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
-                const BItem t = dkdv_item(p, w);
+                const BItem t = dkdv_item(p, w, CAUSAL);
                 ok = mbar_wait(kv_empty, (k & 1) ^ 1, err, SITE_B_PROD_RES);
                 if (!ok) break;
                 mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                     const uint32_t st = qc & 1, ph = (qc >> 1) & 1;
                     ok = mbar_wait(&qo_empty[st], ph ^ 1, err, SITE_B_PROD_RING);
                     if (!ok) break;
-                    const int qt = dkdv_qtile(p, t, it);
+                    const int qt = dkdv_qtile(t, it, CAUSAL);
                     mbar_arrive_expect_tx(&qo_full[st], 2 * C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c) {
                         tma_load_3d(smem + C::kRing0 + st * C::kTileBytes + c * C::kChunkBytes, &p.tq, 64 * c,
@@ -305,14 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const uint32_t sK = smem_u32(smem + C::kRes0), sV = smem_u32(smem + C::kRes1);
             const uint32_t sQ = smem_u32(smem + C::kRing0), sO = smem_u32(smem + C::kRing1);
             const uint64_t kd = smem_desc_sw128(sK, 16, 1024), vd = smem_desc_sw128(sV, 16, 1024);
-            const bool aux = bwd_aux(p, VAR);
+            const bool aux = bwd_aux(CAUSAL, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
             uint32_t qc = 0, pc = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
-                const BItem t = dkdv_item(p, w);
+                const BItem t = dkdv_item(p, w, CAUSAL);
                 ok = mbar_wait(kv_full, k & 1, err, SITE_B_MMA_RES);
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
@@ -376,15 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         for (int k = 0; ok; ++k) {
             const int w = item_index(k);
             if (w >= p.num_items) break;
-            const BItem t = dkdv_item(p, w);
+            const BItem t = dkdv_item(p, w, CAUSAL);
             const float sl2 = p.slopes.log2e[t.bh % p.H];
             const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
-            if (s == 0 && bwd_aux(p, VAR)) {
+            if (s == 0 && bwd_aux(CAUSAL, VAR)) {
                 // column-bias rows (query column c: -m log2(e) c / c1), one item ahead
                 auto publish = [&](int kk) {
                     const int wn = item_index(kk);
                     if (wn >= p.num_items) return;
-                    const BItem tn = dkdv_item(p, wn);
+                    const BItem tn = dkdv_item(p, wn, CAUSAL);
                     write_bias_row(smem + C::kAux, r, kk & 1, -p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             }
             // this lane's share of the column statistics of iteration `it` (prefetched one ahead)
             auto fetch = [&](int it, float (&v)[4]) {
-                const int q0 = dkdv_qtile(p, t, it) * BT + 64 * s;
+                const int q0 = dkdv_qtile(t, it, CAUSAL) * BT + 64 * s;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int i = q0 + lane + 32 * h;
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             float pre[4];
             fetch(0, pre);
             for (int it = 0; it < t.n; ++it) {
-                const int qt = dkdv_qtile(p, t, it);
+                const int qt = dkdv_qtile(t, it, CAUSAL);
                 float *buf = stats + (it & 1) * 128;
                 buf[lane] = pre[0];
                 buf[lane + 32] = pre[1];
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 tmem_wait_ld();
                 // sl2 (i - j) for query i = qt*128 + 64 s + c and key j = jt*128 + r, from integers
                 const float base = sl2 * static_cast<float>((qt - t.tile) * BT + 64 * s - r);
-                const bool diag = p.causal && qt == t.tile;
+                const bool diag = CAUSAL && qt == t.tile;
                 uint32_t pk[32], dk[32];
                 if (VAR) {
                     const float mnat = p.slopes.nat[t.bh % p.H];
@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                             dk[u] = pack_bf16x2(dv[0], dv[1]);
                         }
                     };
-                    if (!p.causal)
+                    if (!CAUSAL)
                         run(std::false_type{}, std::true_type{});
                     else if (diag)
                         run_aux(std::true_type{});
@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 
 // ---------------------------------------------------------------------- dQ
 
-template <int D, bool VAR>
+template <int D, bool VAR, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
     using C = BwdCfg<D>;
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (bwd_aux(p, VAR) && threadIdx.x < 2 * BT) {
+    if (bwd_aux(CAUSAL, VAR) && threadIdx.x < 2 * BT) {
         write_ones_chunk(smem + C::kAux, threadIdx.x >> 1, threadIdx.x & 1);
         fence_proxy_async_smem();
     }
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
-                const BItem t = dq_item(p, w);
+                const BItem t = dq_item(p, w, CAUSAL);
                 ok = mbar_wait(qd_empty, (k & 1) ^ 1, err, SITE_B_PROD_RES);
                 if (!ok) break;
                 mbar_arrive_expect_tx(qd_full, 2 * C::kTileBytes);
@@ -626,14 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             const uint32_t sQ = smem_u32(smem + C::kRes0), sO = smem_u32(smem + C::kRes1);
             const uint32_t sK = smem_u32(smem + C::kRing0), sV = smem_u32(smem + C::kRing1);
             const uint64_t qd = smem_desc_sw128(sQ, 16, 1024), od = smem_desc_sw128(sO, 16, 1024);
-            const bool aux = bwd_aux(p, VAR);
+            const bool aux = bwd_aux(CAUSAL, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
             uint32_t kc = 0, pc = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
-                const BItem t = dq_item(p, w);
+                const BItem t = dq_item(p, w, CAUSAL);
                 ok = mbar_wait(qd_full, k & 1, err, SITE_B_MMA_RES);
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
@@ -688,14 +688,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         for (int k = 0; ok; ++k) {
             const int w = item_index(k);
             if (w >= p.num_items) break;
-            const BItem t = dq_item(p, w);
+            const BItem t = dq_item(p, w, CAUSAL);
             const float sl2 = p.slopes.log2e[t.bh % p.H];
-            if (s == 0 && bwd_aux(p, VAR)) {
+            if (s == 0 && bwd_aux(CAUSAL, VAR)) {
                 // column-bias rows (key column c: m log2(e) c / c1), one item ahead
                 auto publish = [&](int kk) {
                     const int wn = item_index(kk);
                     if (wn >= p.num_items) return;
-                    const BItem tn = dq_item(p, wn);
+                    const BItem tn = dq_item(p, wn, CAUSAL);
                     write_bias_row(smem + C::kAux, r, kk & 1, p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -723,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 tmem_wait_ld();
                 // -sl2 (i - k) for key k = it*128 + 64 s + c, from the integer offset
                 const float nb = -sl2 * static_cast<float>(i - it * BT - 64 * s);
-                const bool diag = p.causal && it == t.tile;
+                const bool diag = CAUSAL && it == t.tile;
                 const float nl = -lse2;
                 uint32_t dk[32];
                 if (VAR) {
@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                             dk[u] = pack_bf16x2(dv[0], dv[1]);
                         }
                     };
-                    if (!p.causal)
+                    if (!CAUSAL)
                         run(std::false_type{}, std::true_type{});
                     else if (diag)
                         run_aux(std::true_type{});
@@ -864,8 +864,10 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     using C = BwdCfg<D>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = check_launch_regs(bwd_dkdv_kernel<D, VAR>, C::kSmem);
-        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D, VAR>, C::kSmem);
+        cudaError_t e = check_launch_regs(bwd_dkdv_kernel<D, VAR, true>, C::kSmem);
+        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D, VAR, true>, C::kSmem);
+        if (e == cudaSuccess) e = check_launch_regs(bwd_dkdv_kernel<D, VAR, false>, C::kSmem);
+        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D, VAR, false>, C::kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -902,11 +904,17 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
 
     p.g0 = static_cast<__nv_bfloat16 *>(dk);
     p.g1 = static_cast<__nv_bfloat16 *>(dv);
-    bwd_dkdv_kernel<D, VAR><<<grid, kThreads, C::kSmem, stream>>>(p);
+    if (causal)
+        bwd_dkdv_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
+    else
+        bwd_dkdv_kernel<D, VAR, false><<<grid, kThreads, C::kSmem, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
-    bwd_dq_kernel<D, VAR><<<grid, kThreads, C::kSmem, stream>>>(p);
+    if (causal)
+        bwd_dq_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
+    else
+        bwd_dq_kernel<D, VAR, false><<<grid, kThreads, C::kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
