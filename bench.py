@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--no-underflow", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     # profiling helpers: run one kernel family on a reduced instance of its workload
-    ap.add_argument("--only", choices=["prefill", "decode", "backward"], default=None)
+    ap.add_argument("--only", choices=["prefill", "decode", "decode_skip", "backward"], default=None)
     ap.add_argument("--prefill-heads", type=int, default=None, help="override H of the prefill workload")
     ap.add_argument("--decode-batch", type=int, default=None, help="override B of the decode workload")
     return ap.parse_args()
@@ -244,7 +244,7 @@ def run_native(args):
     if args.decode_batch:
         wd = gen.Workload(**{**wd.__dict__, "B": args.decode_batch})
     do_pre = args.only in (None, "prefill", "backward")
-    do_dec = args.only in (None, "decode")
+    do_dec = args.only in (None, "decode", "decode_skip")
 
     # Inputs resident in HBM before the timed region. With N ranks the job is a
     # global batch of N x B sequences; each rank fills and runs its contiguous
@@ -299,6 +299,9 @@ def run_native(args):
             dist.destroy_process_group()
         return
 
+    # profiling helper: the skipping decode in place of the dense one (block norms built first)
+    knorm_prof = ab.alibi_kv_block_norms(dk, stream=stream) if args.only == "decode_skip" else None
+
     def step(evs=None):
         flush.fill_(1.0)  # L2 flush, outside the event-timed launches
         if evs:
@@ -308,7 +311,10 @@ def run_native(args):
         if evs:
             evs[1].record(stream)
         if do_dec:
-            ab.alibi_attn_decode(dq, dk, dv, out=dout, stream=stream)
+            if knorm_prof is not None:
+                ab.alibi_attn_decode_skip(dq, dk, dv, knorm_prof, out=dout, stream=stream)
+            else:
+                ab.alibi_attn_decode(dq, dk, dv, out=dout, stream=stream)
         if evs:
             evs[2].record(stream)
 
