@@ -20,8 +20,10 @@
 //   bwd_prep_kernel   D_i = dO_i . O_i (fp32 from the bf16 tensors)
 //   bwd_dkdv_kernel   one work item per (b, h) and 128-key tile: K, V stay in
 //                     shared memory, Q / dO tiles stream through 2-stage rings;
-//                     S^T = K Q^T and dP^T = V dO^T in TMEM, then
-//                     dV += P^T dO and dK += dS^T Q with P^T, dS^T read from TMEM
+//                     S^T = K Q^T and dP^T = V dO^T in TMEM, in two 64-query
+//                     halves pipelined against the two elementwise warpgroups,
+//                     then dV += P^T dO and dK += dS^T Q with P^T, dS^T read
+//                     from TMEM
 //   bwd_dq_kernel     one work item per (b, h) and 128-query tile: Q, dO stay,
 //                     K / V stream; S = Q K^T, dP = dO V^T, dQ += dS K
 // Roles as in the forward kernel: warp 0 TMA producer, warp 1 TMEM allocator
@@ -222,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     uint64_t *kv_empty = bars + 1;
     uint64_t *qo_full = bars + 2;   // [2]
     uint64_t *qo_empty = bars + 4;  // [2]
-    uint64_t *s_full = bars + 6;
-    uint64_t *p_full = bars + 7;
+    uint64_t *s_full = bars + 6;   // [2] S^T and dP^T of query half h in TMEM
+    uint64_t *p_full = bars + 11;  // [2] P^T and dS^T of query half h written back
     uint64_t *acc_full = bars + 8;
     uint64_t *acc_empty = bars + 9;
     uint64_t *mma_done = bars + 10;
@@ -240,8 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             mbar_init(&qo_full[s], 1);
             mbar_init(&qo_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 8);  // one arrival per elementwise warp
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&p_full[h], 4);  // the four warps of the half's warpgroup
+        }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);
         mbar_init(mma_done, 1);
@@ -300,14 +304,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         } else if (warp == 1) {
             // whole warp, converged; one elected lane issues each tcgen05 instruction
             // -------------------------------------------------------- MMA issuer
-            constexpr uint32_t idS = idesc_bf16_f32(BT, BT, 0);
+            // Each query tile is computed in two halves of 64 queries (the columns of one
+            // elementwise warpgroup each): warpgroup 0 starts on its half while the tensor
+            // core computes the other, and each half's dV / dK products go out as soon as
+            // its P^T and dS^T are back, followed by the next tile's S^T / dP^T for that half.
+            constexpr uint32_t idH = idesc_bf16_f32(BT, BT / 2, 0);  // 128 keys x 64 queries
             constexpr uint32_t idG = idesc_bf16_f32(BT, D, 1);
+            constexpr uint32_t kHalfOff = (BT / 2) * 128;              // bytes to query row 64 of a chunk
             const uint32_t sK = smem_u32(smem + C::kRes0), sV = smem_u32(smem + C::kRes1);
             const uint32_t sQ = smem_u32(smem + C::kRing0), sO = smem_u32(smem + C::kRing1);
             const uint64_t kd = smem_desc_sw128(sK, 16, 1024), vd = smem_desc_sw128(sV, 16, 1024);
             const bool aux = bwd_aux(CAUSAL, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
-            uint32_t qc = 0, pc = 0;
+            uint32_t qc = 0, pc[2] = {0, 0};
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
@@ -317,44 +326,71 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                for (int it = 0; it < t.n && ok; ++it, ++qc) {
-                    const uint32_t st = qc & 1, ph = (qc >> 1) & 1;
-                    ok = mbar_wait(&qo_full[st], ph, err, SITE_B_MMA_RING);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // S^T = K Q^T and dP^T = V dO^T (both operands K-major along d)
-                    const uint64_t qd = smem_desc_sw128(sQ + st * C::kTileBytes, 16, 1024);
-                    const uint64_t od = smem_desc_sw128(sO + st * C::kTileBytes, 16, 1024);
+                const uint32_t qb0 = qc;  // ring counter of this item's first query tile
+                auto wait_tile = [&](int it) -> bool {
+                    const uint32_t c = qb0 + it;
+                    bool okw = mbar_wait(&qo_full[c & 1], (c >> 1) & 1, err, SITE_B_MMA_RING);
+                    okw = __all_sync(0xffffffffu, okw);
+                    if (okw) tc_fence_after();
+                    return okw;
+                };
+                // S^T = K Q^T and dP^T = V dO^T for query half h of tile it (operands K-major along d)
+                auto issue_SP = [&](int it, int h) {
+                    const uint32_t st = (qb0 + it) & 1;
+                    const uint64_t qd = smem_desc_sw128(sQ + st * C::kTileBytes + h * kHalfOff, 16, 1024);
+                    const uint64_t od = smem_desc_sw128(sO + st * C::kTileBytes + h * kHalfOff, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_w(tmem + kColS, kd + kmajor_step<D>(kk), qd + kmajor_step<D>(kk), idS, kk > 0);
-                    // column (query) bias: ones x this item's bias rows
-                    if (aux) mma_ss_w(tmem + kColS, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
+                        mma_ss_w(tmem + kColS + 64 * h, kd + kmajor_step<D>(kk), qd + kmajor_step<D>(kk), idH, kk > 0);
+                    // column (query) bias: ones x this item's bias rows 64 h ..
+                    if (aux)
+                        mma_ss_w(tmem + kColS + 64 * h, auxd, auxd + 2 * (1 + (k & 1)) + ((h * kHalfOff) >> 4), idH,
+                                 1u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_w(tmem + kColP, vd + kmajor_step<D>(kk), od + kmajor_step<D>(kk), idS, kk > 0);
-                    mma_commit_w(s_full);
-                    // P^T and dS^T written back by the elementwise warps
-                    ok = mbar_wait(p_full, pc & 1, err, SITE_B_MMA_P);
-                    ++pc;
-                    if (ok && it == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // dV += P^T dO, dK += dS^T Q (B operands MN-major: the contraction runs over queries)
+                        mma_ss_w(tmem + kColP + 64 * h, vd + kmajor_step<D>(kk), od + kmajor_step<D>(kk), idH, kk > 0);
+                    mma_commit_w(&s_full[h]);
+                };
+                // dV += P^T dO and dK += dS^T Q over the 64 queries of half h (B MN-major)
+                auto issue_GG = [&](int it, int h) {
+                    const uint32_t st = (qb0 + it) & 1;
                     const uint64_t omn = smem_desc_sw128(sO + st * C::kTileBytes, C::kChunkBytes, 1024);
                     const uint64_t qmn = smem_desc_sw128(sQ + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int kk = 4 * h + k4;
                         mma_ts_w(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), omn + mnmajor_step(kk), idG,
-                               (it > 0 || kk > 0) ? 1u : 0u);
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+                    }
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int kk = 4 * h + k4;
                         mma_ts_w(tmem + kColAcc1, tmem + tmem_a_col(kColP, kk), qmn + mnmajor_step(kk), idG,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_w(&qo_empty[st]);
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
+                ok = wait_tile(0);
+                if (!ok) break;
+                issue_SP(0, 0);
+                issue_SP(0, 1);
+                for (int it = 0; it < t.n && ok; ++it) {
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        // P^T and dS^T of this half written back by its warpgroup
+                        ok = mbar_wait(&p_full[h], pc[h] & 1, err, SITE_B_MMA_P);
+                        ++pc[h];
+                        if (ok && it == 0 && h == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_GG(it, h);
+                        if (h == 1) mma_commit_w(&qo_empty[(qb0 + it) & 1]);  // tile it read for the last time
+                        if (it + 1 < t.n) {
+                            if (h == 0 && !(ok = wait_tile(it + 1))) break;
+                            issue_SP(it + 1, h);  // over the columns whose P^T / dS^T were just consumed
+                        }
+                    }
                 }
+                qc += t.n;
                 if (!ok) break;
                 mma_commit_w(kv_empty);
                 mma_commit_w(acc_full);
@@ -415,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 buf[64 + lane + 32] = pre[3];
                 __syncwarp();
                 if (it + 1 < t.n) fetch(it + 1, pre);
-                ok = mbar_wait(s_full, s_cnt & 1, err, SITE_B_EW_S);
+                ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_B_EW_S);
                 ++s_cnt;
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -506,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
+                if (lane == 0) mbar_arrive(&p_full[s]);
             }
             if (!ok) break;
             // ------------------------------------------------------ epilogue
