@@ -25,7 +25,8 @@
 //                     then dV += P^T dO and dK += dS^T Q with P^T, dS^T read
 //                     from TMEM
 //   bwd_dq_kernel     one work item per (b, h) and 128-query tile: Q, dO stay,
-//                     K / V stream; S = Q K^T, dP = dO V^T, dQ += dS K
+//                     K / V stream; S = Q K^T, dP = dO V^T (two 64-key halves,
+//                     pipelined the same way), dQ += dS K
 // Roles as in the forward kernel: warp 0 TMA producer, warp 1 TMEM allocator
 // and single-thread MMA issuer, warps 4-7 / 8-11 two elementwise warpgroups
 // that split each tile's 128 columns in halves (TMEM lane = row of the tile).
@@ -582,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     uint64_t *qd_empty = bars + 1;
     uint64_t *kv_full = bars + 2;   // [2]
     uint64_t *kv_empty = bars + 4;  // [2]
-    uint64_t *s_full = bars + 6;
-    uint64_t *p_full = bars + 7;
+    uint64_t *s_full = bars + 6;   // [2] S and dP of key half h in TMEM
+    uint64_t *p_full = bars + 11;  // [2] dS of key half h written back
     uint64_t *acc_full = bars + 8;
     uint64_t *acc_empty = bars + 9;
     uint64_t *mma_done = bars + 10;
@@ -600,8 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 8);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&p_full[h], 4);  // the four warps of the half's warpgroup
+        }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);
         mbar_init(mma_done, 1);
@@ -657,14 +660,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             }
         } else if (warp == 1) {
             // whole warp, converged; one elected lane issues each tcgen05 instruction
-            constexpr uint32_t idS = idesc_bf16_f32(BT, BT, 0);
+            // S and dP in two halves of 64 keys (the columns of one elementwise warpgroup
+            // each); each half's dQ product goes out as soon as its dS is back, followed
+            // by the next tile's S / dP for that half.
+            constexpr uint32_t idH = idesc_bf16_f32(BT, BT / 2, 0);  // 128 queries x 64 keys
             constexpr uint32_t idG = idesc_bf16_f32(BT, D, 1);
+            constexpr uint32_t kHalfOff = (BT / 2) * 128;              // bytes to key row 64 of a chunk
             const uint32_t sQ = smem_u32(smem + C::kRes0), sO = smem_u32(smem + C::kRes1);
             const uint32_t sK = smem_u32(smem + C::kRing0), sV = smem_u32(smem + C::kRing1);
             const uint64_t qd = smem_desc_sw128(sQ, 16, 1024), od = smem_desc_sw128(sO, 16, 1024);
             const bool aux = bwd_aux(CAUSAL, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
-            uint32_t kc = 0, pc = 0;
+            uint32_t kc = 0, pc[2] = {0, 0};
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
@@ -674,38 +681,60 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                for (int it = 0; it < t.n && ok; ++it, ++kc) {
-                    const uint32_t st = kc & 1, ph = (kc >> 1) & 1;
-                    ok = mbar_wait(&kv_full[st], ph, err, SITE_B_MMA_RING);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // S = Q K^T and dP = dO V^T
-                    const uint64_t kd = smem_desc_sw128(sK + st * C::kTileBytes, 16, 1024);
-                    const uint64_t vd = smem_desc_sw128(sV + st * C::kTileBytes, 16, 1024);
+                const uint32_t kb0 = kc;  // ring counter of this item's first key tile
+                auto wait_tile = [&](int it) -> bool {
+                    const uint32_t c = kb0 + it;
+                    bool okw = mbar_wait(&kv_full[c & 1], (c >> 1) & 1, err, SITE_B_MMA_RING);
+                    okw = __all_sync(0xffffffffu, okw);
+                    if (okw) tc_fence_after();
+                    return okw;
+                };
+                // S = Q K^T and dP = dO V^T for key half h of tile it
+                auto issue_SP = [&](int it, int h) {
+                    const uint32_t st = (kb0 + it) & 1;
+                    const uint64_t kd = smem_desc_sw128(sK + st * C::kTileBytes + h * kHalfOff, 16, 1024);
+                    const uint64_t vd = smem_desc_sw128(sV + st * C::kTileBytes + h * kHalfOff, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_w(tmem + kColS, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idS, kk > 0);
-                    // column (key) bias: ones x this item's bias rows
-                    if (aux) mma_ss_w(tmem + kColS, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
+                        mma_ss_w(tmem + kColS + 64 * h, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idH, kk > 0);
+                    // column (key) bias: ones x this item's bias rows 64 h ..
+                    if (aux)
+                        mma_ss_w(tmem + kColS + 64 * h, auxd, auxd + 2 * (1 + (k & 1)) + ((h * kHalfOff) >> 4), idH,
+                                 1u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_w(tmem + kColP, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idS, kk > 0);
-                    mma_commit_w(s_full);
-                    ok = mbar_wait(p_full, pc & 1, err, SITE_B_MMA_P);
-                    ++pc;
-                    if (ok && it == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // dQ += dS K (K MN-major: the contraction runs over keys)
-                    const uint64_t kmn = smem_desc_sw128(sK + st * C::kTileBytes, C::kChunkBytes, 1024);
+                        mma_ss_w(tmem + kColP + 64 * h, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idH, kk > 0);
+                    mma_commit_w(&s_full[h]);
+                };
+                ok = wait_tile(0);
+                if (!ok) break;
+                issue_SP(0, 0);
+                issue_SP(0, 1);
+                for (int it = 0; it < t.n && ok; ++it) {
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        ok = mbar_wait(&p_full[h], pc[h] & 1, err, SITE_B_MMA_P);
+                        ++pc[h];
+                        if (ok && it == 0 && h == 0) ok = mbar_wait(acc_empty, (k & 1) ^ 1, err, SITE_B_MMA_ACC);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // dQ += dS K over the 64 keys of half h (K MN-major: the contraction runs over keys)
+                        const uint32_t st = (kb0 + it) & 1;
+                        const uint64_t kmn = smem_desc_sw128(sK + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_w(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), kmn + mnmajor_step(kk), idG,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_w(&kv_empty[st]);
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const int kk = 4 * h + k4;
+                            mma_ts_w(tmem + kColAcc0, tmem + tmem_a_col(kColS, kk), kmn + mnmajor_step(kk), idG,
+                                     (it > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (h == 1) mma_commit_w(&kv_empty[st]);  // tile it read for the last time
+                        if (it + 1 < t.n) {
+                            if (h == 0 && !(ok = wait_tile(it + 1))) break;
+                            issue_SP(it + 1, h);
+                        }
+                    }
                 }
+                kc += t.n;
                 if (!ok) break;
                 mma_commit_w(qd_empty);
                 mma_commit_w(acc_full);
@@ -746,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             const float lse2 = valid ? p.lse[rowbase + i] * kLog2e : 0.f;
             const float Di = valid ? p.dsum[rowbase + i] : 0.f;
             for (int it = 0; it < t.n; ++it) {
-                ok = mbar_wait(s_full, s_cnt & 1, err, SITE_B_EW_S);
+                ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_B_EW_S);
                 ++s_cnt;
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -829,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
+                if (lane == 0) mbar_arrive(&p_full[s]);
             }
             if (!ok) break;
             ok = mbar_wait(acc_full, k & 1, err, SITE_B_EW_ACC);
