@@ -62,19 +62,20 @@ struct Cfg {
     static constexpr uint32_t kQ = 0;                      // 2 Q tiles
     static constexpr uint32_t kK = 2 * kTileBytes;         // K ring
     static constexpr uint32_t kV = kK + kKStages * kTileBytes;  // V ring
-    // Two 128 x 64 swizzle atoms of bias operands: atom A holds ones (K-step 0, the
-    // A side), the column bias of keys before the rows, +m log2(e) c / c1, for the
-    // two items in flight (K-steps 1, 2), and that of keys after the rows,
-    // -m log2(e) c / c1 (non-causal), for item parity 0 (K-step 3); atom B holds
-    // the latter for parity 1 (K-step 0).
+    // One 128 x 64 swizzle atom of bias operands: ones (K-step 0, the A side), the
+    // column bias m log2(e) c / c1 for the two items in flight (K-steps 1, 2, the B
+    // side), and minus ones (K-step 3, the A side that turns the same column bias
+    // into -m log2(e) c / c1 for keys after the rows, non-causal).
     static constexpr uint32_t kAux = kV + kVStages * kTileBytes;
-    static constexpr uint32_t kAux2 = kAux + kChunkBytes;
-    static constexpr uint32_t kBar = kAux2 + kChunkBytes;
+    // Epilogue staging: 2 KB per softmax warp, one 32 x 32 bf16 box of O at a time.
+    static constexpr uint32_t kStage = kAux + kChunkBytes;
+    static constexpr uint32_t kBar = kStage + kChunkBytes;
     static constexpr uint32_t kSmem = kBar + 256 + 1024;   // barriers, TMEM slot, alignment slack
 };
 
 struct FwdParams {
     CUtensorMap tq, tk, tv;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tout;        // [BH, N, d] bf16, box {32, 32, 1}, no swizzle (epilogue stores)
     __nv_bfloat16 *out;
     float *lse;
     uint32_t *err;
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
         tma_prefetch_desc(&p.tv);
+        tma_prefetch_desc(&p.tout);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (use_aux_bias(p, VAR) && threadIdx.x < 2 * BM) {
         // ones in logical 16-byte chunks 0-1 of every row (the A operand of the bias MMA)
         write_ones_chunk(smem + C::kAux, threadIdx.x >> 1, threadIdx.x & 1);
+        if (!CAUSAL && (threadIdx.x & 1)) write_neg_ones_step3(smem + C::kAux, threadIdx.x >> 1);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -309,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t sV = smem_u32(smem + C::kV);
             const bool aux = use_aux_bias(p, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
-            const uint64_t auxd2 = smem_desc_sw128(smem_u32(smem + C::kAux2), 16, 1024);
             uint32_t kc = 0, vc = 0;
             uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool ok = true;
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (CAUSAL || jt < qt)
                             mma_ss_w(dst, auxd, auxd + 2 * (1 + (k & 1)), idS, 1u);
                         else if (jt > qt)
-                            mma_ss_w(dst, auxd, (k & 1) ? auxd2 : auxd + 6, idS, 1u);
+                            mma_ss_w(dst, auxd + 6, auxd + 2 * (1 + (k & 1)), idS, 1u);  // minus ones
                     }
                     mma_commit_w(&s_full[s]);
                 };
@@ -442,13 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     if (wn >= p.num_items) return;
                     const Item tn = decode_item(p, wn, CAUSAL);
                     const float bv = p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1;
-                    write_bias_row(smem + C::kAux, r, kk & 1, bv);  // keys before the rows
-                    if (!CAUSAL) {  // keys after the rows
-                        if (kk & 1)
-                            write_bias_pair(smem + C::kAux2, r, 0, -bv);
-                        else
-                            write_bias_pair(smem + C::kAux, r, 3, -bv);
-                    }
+                    write_bias_row(smem + C::kAux, r, kk & 1, bv);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bias_full[kk & 1]);
@@ -607,10 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const bool valid = i < p.N;
             // only the D = 64 kernel serves smaller head sizes; D = 128 keeps a compile-time row size
             const int dr = D == 64 ? p.dr : D;
-            __nv_bfloat16 *orow = p.out + (static_cast<size_t>(t.bh) * p.N + (valid ? i : 0)) * dr;
+            // O / l goes out through a per-warp staging box and bulk tensor stores, so the
+            // warp does not wait for its global stores before its next tile (rows past N are
+            // clipped by the tensor map)
+            uint8_t *stg = smem + C::kStage + (warp - 4) * 2048;
+            const int row0 = qt * BM + quad * 32;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                if (c * 32 >= dr) break;  // columns past a smaller head size are zero and not stored
+                if (c * 32 >= dr || row0 >= p.N) break;
                 uint32_t o[32];
                 tmem_ld32(lane_addr + 256 + s * 128 + c * 32, o);
                 tmem_wait_ld();
@@ -618,12 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                 for (int u = 0; u < 16; ++u)
                     b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv_l, __uint_as_float(o[2 * u + 1]) * inv_l);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                    const int n16 = min(4, (dr - c * 32) / 8);  // 16-byte stores in this chunk
+                if (lane == 0) bulk_wait_read();  // the previous box has left the staging
+                __syncwarp();
+                uint4 *dst = reinterpret_cast<uint4 *>(stg + lane * 64);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (u < n16) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&p.tout, stg, c * 32, row0, t.bh);
+                    bulk_commit();
                 }
             }
             tc_fence_before();
@@ -633,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         }
     }
 
+    if (warp >= 4 && lane == 0) bulk_wait_all();  // the epilogue's stores are done
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -656,7 +661,8 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     FwdParams p;
     const uint64_t BH = static_cast<uint64_t>(B) * H;
     if (!encode_tmap_bf16_3d(&p.tq, q, dr, N, BH, 64, BM) || !encode_tmap_bf16_3d(&p.tk, k, dr, N, BH, 64, BN) ||
-        !encode_tmap_bf16_3d(&p.tv, v, dr, N, BH, 64, BN))
+        !encode_tmap_bf16_3d(&p.tv, v, dr, N, BH, 64, BN) ||
+        !encode_tmap_bf16_3d(&p.tout, out, dr, N, BH, 32, 32, false))
         return cudaErrorInvalidValue;
     p.dr = dr;
     p.out = static_cast<__nv_bfloat16 *>(out);

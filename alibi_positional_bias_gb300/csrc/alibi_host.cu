@@ -148,7 +148,7 @@ void fill_slopes_from(int H, const float *nat, Slopes *s)
 }
 
 bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-                         uint32_t box0, uint32_t box1)
+                         uint32_t box0, uint32_t box1, bool swizzle128)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -157,7 +157,8 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint
     const cuuint32_t box[3] = {box0, box1, 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

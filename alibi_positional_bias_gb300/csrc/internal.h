@@ -30,9 +30,10 @@ void fill_slopes_from(int H, const float *nat, Slopes *s);  // caller-chosen slo
 int num_sms();                   // of the current device
 cudaMemPool_t decode_pool();     // library-owned stream-ordered pool of the current device
 // 3-D TMA map over a [dim2, dim1, dim0] bf16 tensor (dim0 fastest), box {box0, box1, 1},
-// 128-byte swizzle, zero fill out of bounds.
+// zero fill out of bounds; 128-byte swizzle, or none (plain row-major boxes, as the
+// epilogue's bulk stores use).
 bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-                         uint32_t box0, uint32_t box1);
+                         uint32_t box0, uint32_t box1, bool swizzle128 = true);
 
 // Decode split plan (alibi_decode.cu): number of KV splits for B*H heads of length L.
 int decode_splits(int BH, int L);

@@ -122,6 +122,25 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
+// 3-D tiled store of one box from shared memory (bulk-group completion). The
+// source must stay unchanged until bulk_wait_read() has returned; rows and columns
+// outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocate `ncols` TMEM columns (whole warp); the base address lands in *dst_smem.
@@ -293,6 +312,15 @@ __device__ __forceinline__ void write_ones_chunk(uint8_t *aux, int r, int j)
 {
     const uint4 v = j == 0 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
     *reinterpret_cast<uint4 *>(aux + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+}
+
+// Row r of K-step 3 (logical chunks 6-7) of the atom that holds the ones: (-1, -1, -1,
+// 0, ...), the A rows that multiply a bias operand into its negation.
+__device__ __forceinline__ void write_neg_ones_step3(uint8_t *aux, int r)
+{
+    uint8_t *row = aux + r * 128;
+    *reinterpret_cast<uint4 *>(row + ((6 ^ (r & 7)) << 4)) = make_uint4(0xBF80BF80u, 0x0000BF80u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(row + ((7 ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Row r of the K-step `pair` (logical chunks 2 pair, 2 pair + 1) of an atom: the
