@@ -63,14 +63,17 @@ struct BwdCfg {
     static constexpr uint32_t kRes1 = kTileBytes;                // V (dKdV) / dO (dQ)
     static constexpr uint32_t kRing0 = 2 * kTileBytes;           // Q / K, 2 stages
     static constexpr uint32_t kRing1 = 4 * kTileBytes;           // dO / V, 2 stages
-    static constexpr uint32_t kStats = 6 * kTileBytes;           // dKdV: per warp 2 x (64 + 64) floats
-    static constexpr uint32_t kAux = kStats + 8 * 2 * 128 * 4;   // bias operands (ptx.cuh), one atom
+    // 2 KB per elementwise warp: dKdV's column statistics (2 x (64 + 64) floats) during
+    // the tile loop, then (both kernels) the epilogue's staging box of 32 x 32 bf16
+    static constexpr uint32_t kStats = 6 * kTileBytes;
+    static constexpr uint32_t kAux = kStats + 8 * 2048;          // bias operands (ptx.cuh), one atom
     static constexpr uint32_t kBar = kAux + kChunkBytes;
     static constexpr uint32_t kSmem = kBar + 256 + 1024;
 };
 
 struct BwdParams {
     CUtensorMap tq, tk, tv, tdo;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tg0, tg1;         // the gradients g0, g1: box {32, 32, 1}, no swizzle (epilogue stores)
     const float *lse;             // [BH, N] natural log (forward output)
     const float *dsum;            // [BH, N] D_i
     __nv_bfloat16 *g0, *g1;       // dKdV: dk, dv; dQ: dq
@@ -186,29 +189,36 @@ __device__ __forceinline__ uint32_t tmem_a_col(uint32_t region, int kk)
     return region + 64 * (kk >> 2) + (kk & 3) * 8;
 }
 
-__device__ __forceinline__ void load_bf16_rows_store(__nv_bfloat16 *row, const uint32_t (&o)[32], float scale)
-{
-    uint32_t b[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u)
-        b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * scale, __uint_as_float(o[2 * u + 1]) * scale);
-    uint4 *dst = reinterpret_cast<uint4 *>(row);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
-}
-
-// Epilogue of one accumulator: this warpgroup's half of d for its thread's row.
+// Epilogue of one accumulator: this warpgroup's half of d for the warp's 32 rows
+// (row0 ..), one 32 x 32 box at a time through the warp's 2 KB staging and a bulk
+// tensor store (rows past N are clipped by the tensor map), so the warp does not
+// wait for its global stores.
 template <int D>
-__device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0, int s, __nv_bfloat16 *row,
-                                               bool valid, float scale)
+__device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0, int s, uint8_t *stg,
+                                               const CUtensorMap *tmap, int row0, int bh, float scale)
 {
     constexpr int kHalf = D / 2;
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_addr + col0 + s * kHalf + c * 32, o);
         tmem_wait_ld();
-        if (valid) load_bf16_rows_store(row + s * kHalf + c * 32, o, scale);
+        uint32_t b[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * scale, __uint_as_float(o[2 * u + 1]) * scale);
+        if (lane == 0) bulk_wait_read();  // the previous box has left the staging
+        __syncwarp();
+        uint4 *dst = reinterpret_cast<uint4 *>(stg + lane * 64);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(tmap, stg, s * kHalf + c * 32, row0, bh);
+            bulk_commit();
+        }
     }
 }
 
@@ -374,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 if (!ok) break;
                 issue_SP(0, 0);
                 issue_SP(0, 1);
+                if (t.n == 1) mma_commit_w(kv_empty);  // K and V read for the last time
                 for (int it = 0; it < t.n && ok; ++it) {
                     for (int h = 0; h < 2 && ok; ++h) {
                         // P^T and dS^T of this half written back by its warpgroup
@@ -388,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                         if (it + 1 < t.n) {
                             if (h == 0 && !(ok = wait_tile(it + 1))) break;
                             issue_SP(it + 1, h);  // over the columns whose P^T / dS^T were just consumed
+                            if (h == 1 && it + 2 == t.n) mma_commit_w(kv_empty);  // K and V read for the last time
                         }
                     }
                 }
                 qc += t.n;
                 if (!ok) break;
-                mma_commit_w(kv_empty);
                 mma_commit_w(acc_full);
             }
             mma_commit_w(mma_done);
@@ -407,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const int r = quad * 32 + lane;  // key row of the tile
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         // per-warp double buffer of the 64 columns' -LSE (base 2) and -D
-        float *stats = reinterpret_cast<float *>(smem + C::kStats) + (warp - 4) * 2 * 128;
+        uint8_t *stg = smem + C::kStats + (warp - 4) * 2048;
+        float *stats = reinterpret_cast<float *>(stg);
         uint32_t s_cnt = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -443,6 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             };
             float pre[4];
             fetch(0, pre);
+            if (lane == 0) bulk_wait_read();  // the previous item's epilogue boxes have left the buffer
+            __syncwarp();
             for (int it = 0; it < t.n; ++it) {
                 const int qt = dkdv_qtile(t, it, CAUSAL);
                 float *buf = stats + (it & 1) * 128;
@@ -551,17 +565,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int j = t.tile * BT + r;
-            const bool valid = j < p.N;
-            const size_t off = (rowbase + (valid ? j : 0)) * D;
-            store_acc_half<D>(lane_addr, kColAcc0, s, p.g1 + off, valid, 1.0f);           // dV
-            store_acc_half<D>(lane_addr, kColAcc1, s, p.g0 + off, valid, p.inv_sqrt_d);   // dK
+            const int row0 = t.tile * BT + quad * 32;
+            if (row0 < p.N) {
+                store_acc_half<D>(lane_addr, kColAcc0, s, stg, &p.tg1, row0, t.bh, 1.0f);          // dV
+                store_acc_half<D>(lane_addr, kColAcc1, s, stg, &p.tg0, row0, t.bh, p.inv_sqrt_d);  // dK
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
         }
     }
 
+    if (warp >= 4 && lane == 0) bulk_wait_all();  // the epilogue's stores are done
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -710,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (!ok) break;
                 issue_SP(0, 0);
                 issue_SP(0, 1);
+                if (t.n == 1) mma_commit_w(qd_empty);  // Q and dO read for the last time
                 for (int it = 0; it < t.n && ok; ++it) {
                     for (int h = 0; h < 2 && ok; ++h) {
                         ok = mbar_wait(&p_full[h], pc[h] & 1, err, SITE_B_MMA_P);
@@ -731,12 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                         if (it + 1 < t.n) {
                             if (h == 0 && !(ok = wait_tile(it + 1))) break;
                             issue_SP(it + 1, h);
+                            if (h == 1 && it + 2 == t.n) mma_commit_w(qd_empty);  // Q and dO read for the last time
                         }
                     }
                 }
                 kc += t.n;
                 if (!ok) break;
-                mma_commit_w(qd_empty);
                 mma_commit_w(acc_full);
             }
             mma_commit_w(mma_done);
@@ -746,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         const int s = (warp - 4) >> 2;  // key columns [64 s, 64 s + 64) of every tile
         const int quad = warp & 3;
+        uint8_t *stg = smem + C::kStats + (warp - 4) * 2048;  // epilogue staging box
         const int r = quad * 32 + lane;  // query row of the tile
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         uint32_t s_cnt = 0;
@@ -865,13 +882,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            store_acc_half<D>(lane_addr, kColAcc0, s, p.g0 + (rowbase + (valid ? i : 0)) * D, valid, p.inv_sqrt_d);
+            const int row0 = t.tile * BT + quad * 32;
+            if (row0 < p.N) store_acc_half<D>(lane_addr, kColAcc0, s, stg, &p.tg0, row0, t.bh, p.inv_sqrt_d);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
         }
     }
 
+    if (warp >= 4 && lane == 0) bulk_wait_all();  // the epilogue's stores are done
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -969,6 +988,9 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
 
     p.g0 = static_cast<__nv_bfloat16 *>(dk);
     p.g1 = static_cast<__nv_bfloat16 *>(dv);
+    if (!encode_tmap_bf16_3d(&p.tg0, dk, D, N, BH, 32, 32, false) ||
+        !encode_tmap_bf16_3d(&p.tg1, dv, D, N, BH, 32, 32, false))
+        return cudaErrorInvalidValue;
     if (causal)
         bwd_dkdv_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else
@@ -976,6 +998,7 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
+    if (!encode_tmap_bf16_3d(&p.tg0, dq, D, N, BH, 32, 32, false)) return cudaErrorInvalidValue;
     if (causal)
         bwd_dq_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else
