@@ -422,12 +422,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         float *stats = reinterpret_cast<float *>(stg);
         uint32_t s_cnt = 0;
         bool ok = true;
+        // this lane's share of the column statistics of item ti's iteration `it`
+        auto fetch = [&](const BItem &ti, int it, float (&v)[4]) {
+            const size_t rb = static_cast<size_t>(ti.bh) * p.N;
+            const int q0 = dkdv_qtile(ti, it, CAUSAL) * BT + 64 * s;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = q0 + lane + 32 * h;
+                const bool in = i < p.N;
+                v[h] = in ? -p.lse[rb + i] * kLog2e : -INFINITY;  // -LSE log2(e); past N: weight 0
+                v[2 + h] = in ? -p.dsum[rb + i] : 0.f;              // -D
+            }
+        };
+        float pre[4];  // prefetched one iteration ahead, across items too
         for (int k = 0; ok; ++k) {
             const int w = item_index(k);
             if (w >= p.num_items) break;
             const BItem t = dkdv_item(p, w, CAUSAL);
             const float sl2 = p.slopes.log2e[t.bh % p.H];
-            const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
+            if (k == 0) fetch(t, 0, pre);
             if (s == 0 && bwd_aux(CAUSAL, VAR)) {
                 // column-bias rows (query column c: -m log2(e) c / c1), one item ahead
                 auto publish = [&](int kk) {
@@ -442,19 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 if (k == 0) publish(0);
                 publish(k + 1);
             }
-            // this lane's share of the column statistics of iteration `it` (prefetched one ahead)
-            auto fetch = [&](int it, float (&v)[4]) {
-                const int q0 = dkdv_qtile(t, it, CAUSAL) * BT + 64 * s;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int i = q0 + lane + 32 * h;
-                    const bool in = i < p.N;
-                    v[h] = in ? -p.lse[rowbase + i] * kLog2e : -INFINITY;  // -LSE log2(e); past N: weight 0
-                    v[2 + h] = in ? -p.dsum[rowbase + i] : 0.f;              // -D
-                }
-            };
-            float pre[4];
-            fetch(0, pre);
             if (lane == 0) bulk_wait_read();  // the previous item's epilogue boxes have left the buffer
             __syncwarp();
             for (int it = 0; it < t.n; ++it) {
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 buf[64 + lane] = pre[2];
                 buf[64 + lane + 32] = pre[3];
                 __syncwarp();
-                if (it + 1 < t.n) fetch(it + 1, pre);
+                if (it + 1 < t.n) fetch(t, it + 1, pre);
                 ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_B_EW_S);
                 ++s_cnt;
                 ok = __all_sync(0xffffffffu, ok);
@@ -561,6 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             }
             if (!ok) break;
             // ------------------------------------------------------ epilogue
+            {  // the next item's first statistics load while this one's gradients go out
+                const int wn = item_index(k + 1);
+                if (wn < p.num_items) fetch(dkdv_item(p, wn, CAUSAL), 0, pre);
+            }
             ok = mbar_wait(acc_full, k & 1, err, SITE_B_EW_ACC);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -763,6 +767,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         const int s = (warp - 4) >> 2;  // key columns [64 s, 64 s + 64) of every tile
         const int quad = warp & 3;
         uint8_t *stg = smem + C::kStats + (warp - 4) * 2048;  // epilogue staging box
+        // this thread's row statistics (LSE log2(e), D) of item ti
+        auto load_stats = [&](const BItem &ti, float (&v)[2]) {
+            const int ii = ti.tile * BT + quad * 32 + lane;
+            const bool in = ii < p.N;
+            const size_t rb = static_cast<size_t>(ti.bh) * p.N;
+            v[0] = in ? p.lse[rb + ii] * kLog2e : 0.f;
+            v[1] = in ? p.dsum[rb + ii] : 0.f;
+        };
+        float nxt[2];  // loaded one item ahead
         const int r = quad * 32 + lane;  // query row of the tile
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         uint32_t s_cnt = 0;
@@ -787,10 +800,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 publish(k + 1);
             }
             const int i = t.tile * BT + r;
-            const bool valid = i < p.N;
-            const size_t rowbase = static_cast<size_t>(t.bh) * p.N;
-            const float lse2 = valid ? p.lse[rowbase + i] * kLog2e : 0.f;
-            const float Di = valid ? p.dsum[rowbase + i] : 0.f;
+            if (k == 0) load_stats(t, nxt);
+            const float lse2 = nxt[0], Di = nxt[1];
             for (int it = 0; it < t.n; ++it) {
                 ok = mbar_wait(&s_full[s], s_cnt & 1, err, SITE_B_EW_S);
                 ++s_cnt;
@@ -878,6 +889,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (lane == 0) mbar_arrive(&p_full[s]);
             }
             if (!ok) break;
+            {  // the next item's row statistics load while this one's dQ goes out
+                const int wn = item_index(k + 1);
+                if (wn < p.num_items) load_stats(dq_item(p, wn, CAUSAL), nxt);
+            }
             ok = mbar_wait(acc_full, k & 1, err, SITE_B_EW_ACC);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
