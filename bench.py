@@ -445,6 +445,17 @@ def run_native(args):
             tf = prefill_flops(wo) / (t_o / 1e3) / 1e12
             others[name] = {"shape": f"B={wo.B} H={wo.H} N={wo.N} d={wo.d}", "ms": t_o, "tflops": world * tf,
                             "frac": tf / peaks["bf16_tflops"]}
+            if name == "layer_n2048":
+                # the decoder-layer training shape's backward (dO ~ N(0, 1) from its own seed)
+                dob = torch.empty_like(to[0])
+                gen.fill_device(gen.Workload(**{**wo.__dict__, "seed": wo.seed + 1}), 0, dob)
+                ab.alibi_attn_fwd(*to, out=oo, lse=lo, stream=stream)
+                go = [torch.empty_like(to[0]) for _ in range(3)]
+                t_ob = timed_ms(lambda: ab.alibi_attn_bwd(*to, oo, lo, dob, *go, stream=stream))
+                tfb = 2.5 * prefill_flops(wo) / (t_ob / 1e3) / 1e12
+                others[name]["backward"] = {"ms": t_ob, "algorithmic_tflops": world * tfb,
+                                            "frac": tfb / peaks["bf16_tflops"]}
+                del dob, go
             del to, oo, lo
 
     # -------------------- decode skipping provably underflowed cache rows (block key norms kept with
