@@ -28,8 +28,10 @@
 //                     K / V stream; S = Q K^T, dP = dO V^T (two 64-key halves,
 //                     pipelined the same way), dQ += dS K
 // Roles as in the forward kernel: warp 0 TMA producer, warp 1 TMEM allocator
-// and single-thread MMA issuer, warps 4-7 / 8-11 two elementwise warpgroups
-// that split each tile's 128 columns in halves (TMEM lane = row of the tile).
+// and MMA issuer (converged, one elected lane issues), warps 4-7 / 8-11 two
+// elementwise warpgroups that split each tile's 128 columns in halves (TMEM
+// lane = row of the tile) and write the gradients through per-warp staging
+// boxes and bulk tensor stores.
 
 #include <cuda.h>
 

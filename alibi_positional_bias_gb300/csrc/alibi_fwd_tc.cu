@@ -14,7 +14,8 @@
 // Design (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: Q tiles once per work item, K/V tiles through
 //               two 2-stage rings (128-byte swizzle, zero fill past N).
-//   warp 1      TMEM allocator and single-thread MMA issuer:
+//   warp 1      TMEM allocator and MMA issuer (converged, one elected lane
+//               issues):
 //                 S_s = Q_s K^T   (128 x 128, fp32 in TMEM, smem x smem)
 //                 O_s += P_s V    (128 x d,   fp32 in TMEM, P read from TMEM)
 //   warps 4-7   softmax for Q tile slot 0, warps 8-11 for slot 1: each thread
@@ -22,6 +23,8 @@
 //               lane), so the row max and row sum need no shuffles. The bias
 //               is generated from the integer tile coordinates; the running
 //               max is raised lazily (only when a tile exceeds it by 2^8).
+//               The same warps write O / l through per-warp staging boxes and
+//               bulk tensor stores.
 // A work item is (b*H + h, block of 256 query rows = two 128-row tiles);
 // KV tiles are visited from the diagonal downwards. Causal: tiles entirely
 // above the diagonal are never loaded. Non-causal: after tile 0 the walk wraps
