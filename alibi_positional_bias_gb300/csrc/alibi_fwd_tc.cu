@@ -37,6 +37,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace alibi {
@@ -482,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // there the distance is |i - k| and the bias -|nb + sl2 c| (sl2 >= 0).
                 const bool sym = !CAUSAL && j >= qt;
                 float x[BN];
+                // rel: x holds the exponent relative to the running max M (the row offset and
+                // -M folded into one FMA); otherwise the absolute exponent
+                bool rel = false;
                 if (VAR) {
                     // Mitigation variants, element by element in base-2 units:
                     //   content  A = s / sqrt(d), soft-capped to z tanh(A / z) with
@@ -510,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 } else if (CAUSAL || j != qt) {
                     // The column part of the bias is already in S (see use_aux_bias); the row
                     // part is nb for keys before the rows and -nb for keys after them.
-                    const float rb = (CAUSAL || j < qt) ? nb : -nb;
+                    rel = it != it0;
+                    const float rb = ((CAUSAL || j < qt) ? nb : -nb) - (rel ? M : 0.f);
                     const float2 rbv = make_float2(rb, rb);
 #pragma unroll
                     for (int u = 0; u < BN / 2; ++u) {
@@ -551,12 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // so the warp rescales together when any of its rows needs it and rows that
                 // do not use alpha = 1. O_s is quiescent here: S_s(it) completing implies
                 // PV_s(it-1), issued before it, has completed.
-                const bool need = (it != it0) && (mt > M + kRescaleThreshold);
+                const bool need = rel ? mt > kRescaleThreshold : (it != it0) && (mt > M + kRescaleThreshold);
                 if (it == it0) M = mt;
                 if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? ex2_approx(M - mt) : 1.0f;
+                    const float alpha = need ? ex2_approx(rel ? -mt : M - mt) : 1.0f;
                     if (need) {
-                        M = mt;
+                        M = rel ? M + mt : mt;
                         l *= alpha;
                     }
 #pragma unroll
@@ -569,28 +575,37 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tmem_st32(lane_addr + 256 + s * 128 + c * 32, o);
                     }
                 }
-                // p = 2^(x - M), packed to bf16 pairs; four independent pair sums
+                // what the exponent still needs subtracted: the new max's rise (relative x), or M
+                const float shift = rel ? (need ? mt : 0.f) : M;
+                // p = 2^(x - shift), packed to bf16 pairs; four independent pair sums
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
-                const float2 negM = make_float2(-M, -M);
                 // Two halves of 64 keys: the first half of P is handed to the MMA issuer
                 // (p_full) while the second half is still being exponentiated (p_hi).
                 uint32_t pk[BN / 2];
+                auto exps = [&](auto sub_c) {
+                    const float2 negs = make_float2(-shift, -shift);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                    for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                    for (int u = half * (BN / 4); u < (half + 1) * (BN / 4); ++u) {
-                        const float2 dv = __fadd2_rn(make_float2(x[2 * u], x[2 * u + 1]), negM);
-                        const float2 pv = make_float2(ex2_approx(dv.x), ex2_approx(dv.y));
-                        acc[u & 3] = __fadd2_rn(acc[u & 3], pv);
-                        pk[u] = pack_bf16x2(pv.x, pv.y);
+                        for (int u = half * (BN / 4); u < (half + 1) * (BN / 4); ++u) {
+                            float2 dv = make_float2(x[2 * u], x[2 * u + 1]);
+                            if (decltype(sub_c)::value) dv = __fadd2_rn(dv, negs);
+                            const float2 pv = make_float2(ex2_approx(dv.x), ex2_approx(dv.y));
+                            acc[u & 3] = __fadd2_rn(acc[u & 3], pv);
+                            pk[u] = pack_bf16x2(pv.x, pv.y);
+                        }
+                        tmem_st32(lane_addr + s * 128 + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[half * 32]));
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(half == 0 ? &p_full[s] : &p_hi[s]);
                     }
-                    tmem_st32(lane_addr + s * 128 + half * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[half * 32]));
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(half == 0 ? &p_full[s] : &p_hi[s]);
-                }
+                };
+                if (__any_sync(0xffffffffu, shift != 0.f))
+                    exps(std::true_type{});
+                else
+                    exps(std::false_type{});
                 const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
                 const float2 a = __fadd2_rn(a01, a23);
                 l += a.x + a.y;
