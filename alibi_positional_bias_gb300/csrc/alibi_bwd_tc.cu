@@ -54,6 +54,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // TMEM columns (both main kernels): accumulators at 0 and 128 (dV, dK or dQ),
 // S / S^T at 256 (P or dS bf16 written over its halves), dP / dP^T at 384.
 constexpr uint32_t kColAcc0 = 0, kColAcc1 = 128, kColS = 256, kColP = 384;
+// dQ kernel: the item's Q and dO, copied from shared memory into the columns the
+// second accumulator takes in the dK/dV kernel, as the A operands of S and dP
+// (bf16 pairs, K-step kk at + 8 kk): 128 x 64 products with A in TMEM read only B
+// from shared memory and run at the tensor rate.
+constexpr uint32_t kColQ = 128, kColDO = 192;
 
 template <int D>
 struct BwdCfg {
@@ -702,6 +707,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_B_MMA_RES);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+                tc_fence_after();
+                // Q and dO into TMEM (after the previous item's MMAs in issue order); the
+                // shared-memory copies are free once these complete
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    tmem_cp_w(tmem + kColQ + 8 * kk, qd + kmajor_step<D>(kk));
+                    tmem_cp_w(tmem + kColDO + 8 * kk, od + kmajor_step<D>(kk));
+                }
+                mma_commit_w(qd_empty);
                 const uint32_t kb0 = kc;  // ring counter of this item's first key tile
                 auto wait_tile = [&](int it) -> bool {
                     const uint32_t c = kb0 + it;
@@ -710,28 +724,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                     if (okw) tc_fence_after();
                     return okw;
                 };
-                // S = Q K^T and dP = dO V^T for key half h of tile it
+                // S = Q K^T and dP = dO V^T for key half h of tile it: A (Q, dO) from TMEM,
+                // B (the half's 64 keys) K-major from the ring
                 auto issue_SP = [&](int it, int h) {
                     const uint32_t st = (kb0 + it) & 1;
                     const uint64_t kd = smem_desc_sw128(sK + st * C::kTileBytes + h * kHalfOff, 16, 1024);
                     const uint64_t vd = smem_desc_sw128(sV + st * C::kTileBytes + h * kHalfOff, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_w(tmem + kColS + 64 * h, qd + kmajor_step<D>(kk), kd + kmajor_step<D>(kk), idH, kk > 0);
+                        mma_ts_w(tmem + kColS + 64 * h, tmem + kColQ + 8 * kk, kd + kmajor_step<D>(kk), idH, kk > 0);
                     // column (key) bias: ones x this item's bias rows 64 h ..
                     if (aux)
                         mma_ss_w(tmem + kColS + 64 * h, auxd, auxd + 2 * (1 + (k & 1)) + ((h * kHalfOff) >> 4), idH,
                                  1u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_w(tmem + kColP + 64 * h, od + kmajor_step<D>(kk), vd + kmajor_step<D>(kk), idH, kk > 0);
+                        mma_ts_w(tmem + kColP + 64 * h, tmem + kColDO + 8 * kk, vd + kmajor_step<D>(kk), idH, kk > 0);
                     mma_commit_w(&s_full[h]);
                 };
                 ok = wait_tile(0);
                 if (!ok) break;
                 issue_SP(0, 0);
                 issue_SP(0, 1);
-                if (t.n == 1) mma_commit_w(qd_empty);  // Q and dO read for the last time
                 for (int it = 0; it < t.n && ok; ++it) {
                     for (int h = 0; h < 2 && ok; ++h) {
                         ok = mbar_wait(&p_full[h], pc[h] & 1, err, SITE_B_MMA_P);
@@ -753,7 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                         if (it + 1 < t.n) {
                             if (h == 0 && !(ok = wait_tile(it + 1))) break;
                             issue_SP(it + 1, h);
-                            if (h == 1 && it + 2 == t.n) mma_commit_w(qd_empty);  // Q and dO read for the last time
                         }
                     }
                 }

@@ -204,6 +204,20 @@ __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// Copy a 128-row x 32-byte slice of a shared-memory matrix (described like an MMA
+// operand: swizzle, strides, K-step offset) into TMEM: row r to lane r, the 16 bf16
+// of the slice as 8 columns of bf16 pairs, the layout an A operand read from TMEM
+// takes. Ordered with the issuing thread's MMAs; tracked by its commits.
+__device__ __forceinline__ void tmem_cp_w(uint32_t taddr, uint64_t s_desc)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(s_desc)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
