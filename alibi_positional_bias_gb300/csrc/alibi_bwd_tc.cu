@@ -24,8 +24,9 @@
 //                     halves pipelined against the two elementwise warpgroups,
 //                     then dV += P^T dO and dK += dS^T Q with P^T, dS^T read
 //                     from TMEM
-//   bwd_dq_kernel     one work item per (b, h) and 128-query tile: Q, dO stay,
-//                     K / V stream; S = Q K^T, dP = dO V^T (two 64-key halves,
+//   bwd_dq_kernel     one work item per (b, h) and 128-query tile: Q, dO are
+//                     copied into TMEM (tcgen05.cp), K / V stream; S = Q K^T,
+//                     dP = dO V^T with A from TMEM (two 64-key halves,
 //                     pipelined the same way), dQ += dS K
 // Roles as in the forward kernel: warp 0 TMA producer, warp 1 TMEM allocator
 // and MMA issuer (converged, one elected lane issues), warps 4-7 / 8-11 two
@@ -65,7 +66,8 @@ struct BwdCfg {
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kChunkBytes = BT * 128;
     static constexpr uint32_t kTileBytes = BT * D * 2;
-    // dKdV: K, V resident; Q, dO rings. dQ: Q, dO resident; K, V rings. Same layout:
+    // dKdV: K, V resident; Q, dO rings. dQ: Q, dO staged (then copied into TMEM); K, V
+    // rings. Same layout:
     static constexpr uint32_t kRes0 = 0;                         // K (dKdV) / Q (dQ)
     static constexpr uint32_t kRes1 = kTileBytes;                // V (dKdV) / dO (dQ)
     static constexpr uint32_t kRing0 = 2 * kTileBytes;           // Q / K, 2 stages
