@@ -248,19 +248,31 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restri
     for (int s = lane; s < splits; s += 32) M = fmaxf(M, base[s * kStride]);
 #pragma unroll
     for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (4 * lane >= D) return;
+    // lanes own 4 output columns each; the partials of 8 splits are loaded together
+    const bool mine = 4 * lane < D;
     float Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < splits; ++s) {
-        const float *ps = base + s * kStride;
-        const float ms = ps[0];
-        const float a = (ms == -INFINITY) ? 0.f : ex2_approx(ms - M);
-        Lsum = fmaf(ps[1], a, Lsum);
-        const float4 ov = *reinterpret_cast<const float4 *>(ps + 4 + 4 * lane);
-        O[0] = fmaf(ov.x, a, O[0]);
-        O[1] = fmaf(ov.y, a, O[1]);
-        O[2] = fmaf(ov.z, a, O[2]);
-        O[3] = fmaf(ov.w, a, O[3]);
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+        float ms[8], ls[8];
+        float4 ov[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool in = s0 + j < splits;
+            const float *ps = base + (in ? s0 + j : 0) * kStride;
+            ms[j] = in ? ps[0] : -INFINITY;
+            ls[j] = in ? ps[1] : 0.f;
+            ov[j] = (in && mine) ? *reinterpret_cast<const float4 *>(ps + 4 + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float a = (ms[j] == -INFINITY) ? 0.f : ex2_approx(ms[j] - M);
+            Lsum = fmaf(ls[j], a, Lsum);
+            O[0] = fmaf(ov[j].x, a, O[0]);
+            O[1] = fmaf(ov[j].y, a, O[1]);
+            O[2] = fmaf(ov[j].z, a, O[2]);
+            O[3] = fmaf(ov[j].w, a, O[3]);
+        }
     }
+    if (!mine) return;
     const float inv = 1.0f / Lsum;
     __nv_bfloat162 r0 = __floats2bfloat162_rn(O[0] * inv, O[1] * inv);
     __nv_bfloat162 r1 = __floats2bfloat162_rn(O[2] * inv, O[3] * inv);
@@ -331,14 +343,27 @@ cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, in
 
 // Split count: enough CTAs for several waves (two resident per SM), at least
 // 512 keys per split, and every split non-empty.
+// Split count: with at least as many heads as resident CTAs (two per SM) every SM
+// streams whole heads and there is nothing to merge; with fewer, the cache of each
+// head is cut into the number of slices that minimises (waves of CTAs) x (keys per
+// CTA + a fixed per-CTA cost of 256 keys) plus the merge, slices of at least 256 keys.
 int decode_splits(int BH, int L)
 {
-    const int target = 8 * 2 * num_sms();
-    int splits = (target + BH - 1) / BH;
-    const int max_by_len = (L + 511) / 512;
-    if (splits > max_by_len) splits = max_by_len;
-    if (splits < 1) splits = 1;
-    return splits;
+    const long long R = 2LL * num_sms();
+    if (BH >= R) return 1;
+    const int max_s = (L + 255) / 256;
+    int best = 1;
+    long long best_cost = -1;
+    for (int s = 1; s <= max_s && s <= 4096; ++s) {
+        const long long waves = (static_cast<long long>(BH) * s + R - 1) / R;
+        // a split also costs its merge: a second launch and the partials (~512 keys)
+        const long long cost = waves * ((L + s - 1) / s + 256) + (s > 1 ? 512 : 0);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
 }
 
 size_t decode_partials_bytes(int BH, int splits, int d)
