@@ -343,14 +343,15 @@ cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, in
 
 // Split count: enough CTAs for several waves (two resident per SM), at least
 // 512 keys per split, and every split non-empty.
-// Split count: with at least as many heads as resident CTAs (two per SM) every SM
-// streams whole heads and there is nothing to merge; with fewer, the cache of each
-// head is cut into the number of slices that minimises (waves of CTAs) x (keys per
-// CTA + a fixed per-CTA cost of 256 keys) plus the merge, slices of at least 256 keys.
+// Split count: with eight or more waves of whole heads (two resident CTAs per SM)
+// every SM streams whole heads and there is nothing to merge; with fewer, each
+// head's cache is cut into the number of slices that minimises (waves of CTAs) x
+// (keys per CTA + a fixed per-CTA cost of 256 keys) plus the merge, slices of at
+// least 256 keys.
 int decode_splits(int BH, int L)
 {
     const long long R = 2LL * num_sms();
-    if (BH >= R) return 1;
+    if (BH >= 8 * R) return 1;
     const int max_s = (L + 255) / 256;
     int best = 1;
     long long best_cost = -1;
