@@ -11,8 +11,8 @@
 // loads. A group of d/8 lanes owns one key row (8 bf16 per lane: 16 lanes for
 // d = 128, 8 for 64, 4 for 32, 2 for 16), so a warp-wide load covers 32/(d/8)
 // adjacent rows (512 contiguous bytes). Each lane issues 8 K and 8 V loads
-// before using them, keeping ~8 KB per warp in flight at every d. Grid =
-// (splits, B*H); each CTA (8 warps) streams a contiguous slice of the cache,
+// before using them, keeping ~8 KB per warp in flight at every d. One CTA per
+// (b, h) and split (one-dimensional grid, splits of a head adjacent); each CTA (8 warps) streams a contiguous slice of the cache,
 // merges its warps' partial softmaxes in shared memory, and either writes the
 // output (one split) or an fp32 partial (m, l, o[d]) that a second kernel
 // merges.
@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane / LPR, l16 = lane % LPR;  // lane group (key row) and slice within the row
-    const int bh = blockIdx.y, split = blockIdx.x;
+    // one-dimensional grid (B*H may exceed the 65535 limit of the y dimension): the
+    // splits of one (b, h) are adjacent
+    const int bh = static_cast<int>(blockIdx.x / p.splits), split = static_cast<int>(blockIdx.x - bh * p.splits);
     const int h = bh % p.H;
     const float sl2 = p.slopes.log2e[h];
     const int pos = p.L - 1;
@@ -282,8 +284,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restri
     *reinterpret_cast<uint2 *>(out + static_cast<size_t>(warp) * D + 4 * lane) = pk;
 }
 
-// Maximum key norm of each 64-key block of the cache: grid (blocks, B*H), 256
-// threads, d/8 lanes per key. Blocks [blk_begin, nblk) of every (b, h).
+// Maximum key norm of each 64-key block of the cache: one CTA per (b, h) and block
+// (one-dimensional grid), 256 threads, d/8 lanes per key. Blocks [blk_begin, nblk) of every (b, h).
 template <int D>
 __global__ void __launch_bounds__(256) kv_block_norms_kernel(const __nv_bfloat16 *__restrict__ k, float *__restrict__ knorm,
                                                              int L, int nblk, int blk_begin)
@@ -291,7 +293,8 @@ __global__ void __launch_bounds__(256) kv_block_norms_kernel(const __nv_bfloat16
     constexpr int LPR = D / 8, RPW = 32 / LPR;
     __shared__ float red[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blk_begin + blockIdx.x, bh = blockIdx.y;
+    const int nb = nblk - blk_begin;  // one-dimensional grid: the blocks of one (b, h) are adjacent
+    const int bh = static_cast<int>(blockIdx.x / nb), b = blk_begin + static_cast<int>(blockIdx.x - bh * nb);
     const int g = lane / LPR, l = lane % LPR;
     const __nv_bfloat16 *kb = k + static_cast<size_t>(bh) * L * D + 8 * l;
     float best = 0.f;
@@ -329,7 +332,9 @@ cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, in
 {
     const int nblk = (L + 63) / 64;
     if (blk_begin >= nblk) return cudaSuccess;
-    dim3 grid(nblk - blk_begin, B * H);
+    const long long nblocks = static_cast<long long>(nblk - blk_begin) * B * H;
+    if (nblocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(nblocks);
     const auto *k = static_cast<const __nv_bfloat16 *>(kc);
     switch (d) {
         case 128: kv_block_norms_kernel<128><<<grid, 256, 0, stream>>>(k, knorm, L, nblk, blk_begin); break;
@@ -398,7 +403,9 @@ static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc
     // recompute splits so that no split is empty after rounding the chunk
     p.splits = (L + p.chunk - 1) / p.chunk;
     if (p.splits > splits) return cudaErrorInvalidValue;
-    dim3 grid(p.splits, BH);
+    const long long nblocks = static_cast<long long>(p.splits) * BH;
+    if (nblocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(nblocks);
     decode_kernel<D><<<grid, kWarps * 32, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;

@@ -131,8 +131,10 @@ __global__ void __launch_bounds__(kUfRows) underflow_kernel(const __nv_bfloat16 
 {
     __shared__ __align__(16) float ks[kUfKeys][D];
     __shared__ unsigned long long red[kUfRows / 32];
-    const int bh = blockIdx.y;
-    const int r0 = blockIdx.x * kUfRows;
+    // one-dimensional grid (B*H may exceed the 65535 limit of the y dimension)
+    const int nrb = (N + kUfRows - 1) / kUfRows;
+    const int bh = static_cast<int>(blockIdx.x / nrb);
+    const int r0 = static_cast<int>(blockIdx.x - bh * nrb) * kUfRows;
     const int i = r0 + threadIdx.x;
     const bool valid = i < N;
     const float slope = slopes.nat[bh % H];
@@ -257,7 +259,9 @@ cudaError_t launch_underflow(const void *q, const void *k, int B, int H, int N, 
 {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * H, stream);
     if (e != cudaSuccess) return e;
-    dim3 grid((N + kUfRows - 1) / kUfRows, B * H);
+    const long long nblocks = static_cast<long long>((N + kUfRows - 1) / kUfRows) * B * H;
+    if (nblocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(nblocks);
     const float scale = 1.0f / sqrtf(static_cast<float>(d));
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);

@@ -76,3 +76,22 @@ def test_decode_full_size_sampled_heads(ab):
         vh = gen.head_slice(w, 2, b, h)
         ro, _ = oracle.decode(qh.f32[None, None], kh.f32[None, None], vh.f32[None, None], m=m[h:h + 1])
         assert_bf16_out(out[b, h], ro[0, 0], what=f"out[{b},{h}]")
+
+
+def test_decode_more_heads_than_grid_rows(ab):
+    # B*H = 71680 (b, h) pairs: more than the 65535 rows a y grid dimension can hold;
+    # dense and skipping decode both against the oracle, every head
+    B, H, L, d = 1024, 70, 20, 16
+    w = gen.Workload("dec", "decode", B, H, L, d, "bf16", seed=91)
+    q, k, v = gen.generate(w)
+    qd, kd, vd = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    out = ab.alibi_attn_decode(qd, kd, vd)
+    knorm = ab.alibi_kv_block_norms(kd)
+    out_s = ab.alibi_attn_decode_skip(qd, kd, vd, knorm)
+    ab.alibi_check_error()
+    ro, _ = oracle.decode(q.f32, k.f32, v.f32)
+    assert_bf16_out(host64(out), ro)
+    assert_bf16_out(host64(out_s), ro)
+    # block norms of the last (b, h), computed directly
+    kl = k.f32[-1, -1].astype(np.float64)
+    assert abs(float(knorm[-1, -1, 0]) - np.sqrt((kl * kl).sum(axis=1)).max()) <= 1e-5 * np.sqrt((kl * kl).sum(axis=1)).max()

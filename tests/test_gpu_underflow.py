@@ -58,3 +58,13 @@ def test_zero_logits_closed_form_full_size(ab):
         want = (N - w) * (N - w + 1) // 2 if w < N else 0
         # exact except where m D lands within rounding of tau for some distance D
         assert abs(int(c[h]) - want) <= N, (h, int(c[h]), want)
+
+
+def test_counts_more_heads_than_grid_rows(ab):
+    # B*H = 70000 (b, h) pairs: more than the 65535 rows a y grid dimension can hold
+    w = gen.Workload("uf", "prefill", 700, 100, 8, 16, "bf16", seed=17)
+    q, k, _ = gen.generate(w)
+    got = gpu_counts(ab, q, k)
+    want, near = oracle.underflow_counts_per_head(q.f32, k.f32, TAU_D, band=band_for(w.H, w.N))
+    diff = np.abs(got - want.astype(np.int64))
+    assert (diff <= near.astype(np.int64)).all(), (got, want, near)
