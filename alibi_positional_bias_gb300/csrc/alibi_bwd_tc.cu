@@ -82,7 +82,7 @@ struct BwdCfg {
 
 struct BwdParams {
     CUtensorMap tq, tk, tv, tdo;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
-    CUtensorMap tg0, tg1;         // the gradients g0, g1: box {32, 32, 1}, no swizzle (epilogue stores)
+    CUtensorMap tg0, tg1;         // the gradients g0, g1: box {16, 32, 1}, no swizzle (epilogue stores)
     const float *lse;             // [BH, N] natural log (forward output)
     const float *dsum;            // [BH, N] D_i
     __nv_bfloat16 *g0, *g1;       // dKdV: dk, dv; dQ: dq
@@ -199,9 +199,10 @@ __device__ __forceinline__ uint32_t tmem_a_col(uint32_t region, int kk)
 }
 
 // Epilogue of one accumulator: this warpgroup's half of d for the warp's 32 rows
-// (row0 ..), one 32 x 32 box at a time through the warp's 2 KB staging and a bulk
-// tensor store (rows past N are clipped by the tensor map), so the warp does not
-// wait for its global stores.
+// (row0 ..), as 32 x 16 boxes through the two 1 KB halves of the warp's staging in
+// turn and bulk tensor stores (rows past N are clipped by the tensor map), so the
+// warp neither waits for its global stores nor for each box to leave before
+// writing the next.
 template <int D>
 __device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0, int s, uint8_t *stg,
                                                const CUtensorMap *tmap, int row0, int bh, float scale)
@@ -217,16 +218,20 @@ __device__ __forceinline__ void store_acc_half(uint32_t lane_addr, uint32_t col0
 #pragma unroll
         for (int u = 0; u < 16; ++u)
             b[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * scale, __uint_as_float(o[2 * u + 1]) * scale);
-        if (lane == 0) bulk_wait_read();  // the previous box has left the staging
-        __syncwarp();
-        uint4 *dst = reinterpret_cast<uint4 *>(stg + lane * 64);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_3d(tmap, stg, s * kHalf + c * 32, row0, bh);
-            bulk_commit();
+        for (int hb = 0; hb < 2; ++hb) {  // two 32 x 16 boxes, the staging's two halves in turn
+            uint8_t *buf = stg + hb * 1024;
+            if (lane == 0) bulk_wait_read1();  // the box before the previous one has left
+            __syncwarp();
+            uint4 *dst = reinterpret_cast<uint4 *>(buf + lane * 32);
+            dst[0] = make_uint4(b[8 * hb], b[8 * hb + 1], b[8 * hb + 2], b[8 * hb + 3]);
+            dst[1] = make_uint4(b[8 * hb + 4], b[8 * hb + 5], b[8 * hb + 6], b[8 * hb + 7]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(tmap, buf, s * kHalf + c * 32 + hb * 16, row0, bh);
+                bulk_commit();
+            }
         }
     }
 }
@@ -1020,8 +1025,8 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
 
     p.g0 = static_cast<__nv_bfloat16 *>(dk);
     p.g1 = static_cast<__nv_bfloat16 *>(dv);
-    if (!encode_tmap_bf16_3d(&p.tg0, dk, D, N, BH, 32, 32, false) ||
-        !encode_tmap_bf16_3d(&p.tg1, dv, D, N, BH, 32, 32, false))
+    if (!encode_tmap_bf16_3d(&p.tg0, dk, D, N, BH, 16, 32, false) ||
+        !encode_tmap_bf16_3d(&p.tg1, dv, D, N, BH, 16, 32, false))
         return cudaErrorInvalidValue;
     if (causal)
         bwd_dkdv_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
@@ -1030,7 +1035,7 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
-    if (!encode_tmap_bf16_3d(&p.tg0, dq, D, N, BH, 32, 32, false)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16_3d(&p.tg0, dq, D, N, BH, 16, 32, false)) return cudaErrorInvalidValue;
     if (causal)
         bwd_dq_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else
