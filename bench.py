@@ -460,7 +460,7 @@ def run_native(args):
 
     # -------------------- decode skipping provably underflowed cache rows (block key norms kept with
     # the cache; computed once here, outside the timed loop, as a serving loop would keep them)
-    dskip = None
+    dskip = single = None
     if do_dec:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
@@ -483,6 +483,28 @@ def run_native(args):
         dskip = {"ms": t_ds, "effective_gbs": world * decode_bytes(wd) / (t_ds / 1e3) / 1e9, "unit": "GB/s",
                  "rows_skipped_frac": skipped, "block_norms_ms_once": norm_ms,
                  "exact": "omitted weights < 2^-127 of the largest; matches the dense decode to bf16 rounding (tested)"}
+
+        # -------------------- one sequence (B=1) of the same decode layer: latency per call,
+        # issued directly and replayed from a CUDA graph (a serving loop's decode step)
+        w1 = gen.Workload(**{**wd.__dict__, "B": 1})
+        s1 = [torch.empty(w1.shapes()[i], dtype=torch.bfloat16, device=dev) for i in range(3)]
+        for i, t_ in enumerate(s1):
+            gen.fill_device(w1, i, t_)
+        o1 = torch.empty(s1[0].shape, dtype=torch.bfloat16, device=dev)
+        t_direct = timed_ms(lambda: ab.alibi_attn_decode(*s1, out=o1, stream=stream))
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            ab.alibi_attn_decode(*s1, out=o1)  # warm the pool on the capture stream
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            ab.alibi_attn_decode(*s1, out=o1)
+        t_graph = timed_ms(lambda: graph.replay())
+        single = {"shape": f"B=1 H={wd.H} L={wd.N} d={wd.d}", "splits": ab.alibi_attn_decode_splits(1, wd.H, wd.N, wd.d),
+                  "us_direct": 1e3 * t_direct, "us_graph": 1e3 * t_graph,
+                  "gbs_graph": decode_bytes(w1) / (t_graph / 1e3) / 1e9}
+        del s1, o1, graph
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
@@ -637,6 +659,7 @@ def run_native(args):
         "backward": backward,
         "prefill_other_configs": others,
         "decode_skip_underflow": dskip,
+        "decode_single_sequence": single,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
