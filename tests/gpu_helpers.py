@@ -59,3 +59,17 @@ def sample_rows(B: int, H: int, N: int, max_heads: int = 8, per_head: int = 24, 
         rr |= set(rng.integers(0, N, size=per_head).tolist())
         rows.extend(int(bh) * N + i for i in sorted(rr))
     return np.array(rows, dtype=np.int64)
+
+
+def assert_grad(got: np.ndarray, ref: np.ndarray, rel: float, what: str, bf16: bool = False):
+    """Per (b, h): |got - ref| <= rel * max(1, max |ref|) (+ half a bf16 ulp of ref for bf16 results)."""
+    B, H = ref.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            g, r = got[b, h], ref[b, h]
+            scale = max(1.0, float(np.abs(r).max()))
+            lim = rel * scale + (half_ulp_bf16(r) if bf16 else 0.0)
+            err = np.abs(g - r)
+            assert np.isfinite(g).all(), f"{what}[{b},{h}]: non-finite"
+            assert (err <= lim).all(), (f"{what}[{b},{h}]: max err {err.max():.3e}, scale {scale:.3e}, "
+                                        f"worst excess {(err - lim).max():.3e}")

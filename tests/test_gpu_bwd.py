@@ -16,7 +16,7 @@ import pytest
 
 import alibi_inputs as gen
 import oracle
-from gpu_helpers import dev, half_ulp_bf16, host64
+from gpu_helpers import assert_grad, dev, host64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,17 +31,7 @@ def ab():
     return ab
 
 
-def check_grad(got, ref, rel, what, bf16=False):
-    B, H = ref.shape[:2]
-    for b in range(B):
-        for h in range(H):
-            g, r = got[b, h], ref[b, h]
-            scale = max(1.0, float(np.abs(r).max()))
-            lim = rel * scale + (half_ulp_bf16(r) if bf16 else 0.0)
-            err = np.abs(g - r)
-            assert np.isfinite(g).all(), f"{what}[{b},{h}]: non-finite"
-            assert (err <= lim).all(), (f"{what}[{b},{h}]: max err {err.max():.3e}, scale {scale:.3e}, "
-                                        f"worst excess {(err - lim).max():.3e}")
+check_grad = assert_grad
 
 
 def cases(seed, B, H, N, d, dtype):

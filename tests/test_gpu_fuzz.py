@@ -1,0 +1,160 @@
+"""Seeded random configurations of every bf16 path against the oracle.
+
+The fixed tests pin chosen shapes and options one at a time; these cross them:
+random batch, heads, sequence length (uniform on a log scale, or one key either
+side of a 128-row tile edge), every head size, both masks ("ALiBi and Relative
+Position Bias", "The mechanics", for the symmetric one), exact underflow
+skipping, the mitigations of "When Attention Goes Blind" sec. 3.4 with random
+parameters, and the robust slopes of its sec. 3.4 "Robust Slopes". The cases
+are drawn once from a fixed seed, so every run checks the same ones.
+
+V is drawn from U(-1, 1), as in the long-context workload: the bf16 P V product
+rounds each weight with unit roundoff 2^-8, which moves an output by up to
+2^-8 max|v| before its own rounding, so the 1e-2 bound on the bf16 output holds
+for values of order one; with N(0, 1) values and peaked weights (large logits)
+an output near 4 may legitimately miss it by its own P rounding.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import alibi_inputs as gen
+import oracle
+from gpu_helpers import TOL_BF16_LSE, assert_bf16_out, assert_close, assert_grad, dev, host64
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16_REL = 2.0 ** -5  # gradients: relative to each head's largest gradient entry
+
+ABI = {"clamp": 2, "logdist": 4, "softcap": 8}
+ORC = {"clamp": oracle.CLAMP, "logdist": oracle.LOGDIST, "softcap": oracle.SOFTCAP}
+COMBOS = [c for r in (1, 2, 3) for c in itertools.combinations(("clamp", "logdist", "softcap"), r)]
+
+
+def _length(rng, top):
+    if rng.random() < 0.4:  # one key either side of a tile edge, or on it
+        return int(min(top, max(1, 128 * int(rng.integers(1, top // 128 + 1)) + int(rng.integers(-1, 2)))))
+    return int(min(top, max(1, round(np.exp(rng.uniform(0.0, np.log(top)))))))
+
+
+def _options(rng, causal, H, allow_skip):
+    """mode, flag combination, clamp_min, softcap_z and (optional) explicit slopes."""
+    modes = ["plain", "variant", "slopes"] + (["skip", "skip_slopes"] if causal and allow_skip else [])
+    mode = str(rng.choice(modes))
+    combo = COMBOS[int(rng.integers(len(COMBOS)))] if mode == "variant" else ()
+    clamp_min = float(rng.choice([-87.0, -3.0, float(-rng.uniform(1.0, 20.0))]))
+    softcap_z = float(rng.uniform(4.0, 50.0))
+    delta = None
+    if mode in ("slopes", "skip_slopes") or (mode == "variant" and rng.random() < 0.3):
+        d0 = float(np.exp(rng.uniform(np.log(8.0), np.log(512.0))))
+        delta = (d0, float(d0 * np.exp(rng.uniform(0.0, np.log(64.0)))))
+    return mode, combo, clamp_min, softcap_z, delta
+
+
+def _fwd_cases(n=36, seed=20261202):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        causal = True if i % 3 == 0 else bool(rng.integers(2))
+        d = int(rng.choice([16, 32, 64, 128]))
+        N = _length(rng, 1200)
+        B, H = int(rng.integers(1, 4)), int(rng.integers(1, 9))
+        sigma = float(rng.choice([1.0, 3.0]))
+        mode, combo, cmin, z, delta = _options(rng, causal, H, allow_skip=True)
+        out.append(pytest.param(i, causal, B, H, N, d, sigma, mode, combo, cmin, z, delta,
+                                id=f"{i:02d}-{'c' if causal else 'nc'}-B{B}H{H}N{N}d{d}-{mode}{'+'.join(combo)}"))
+    return out
+
+
+@pytest.fixture(scope="module")
+def ab():
+    import alibi_positional_bias_gb300 as ab
+    ab.load()
+    return ab
+
+
+def _slopes(ab, H, delta):
+    return None if delta is None else ab.alibi_slopes_explicit(H, delta[0], delta[1])
+
+
+@pytest.mark.parametrize("i,causal,B,H,N,d,sigma,mode,combo,cmin,z,delta", _fwd_cases())
+def test_prefill_random_configurations(ab, i, causal, B, H, N, d, sigma, mode, combo, cmin, z, delta):
+    q, k, _ = gen.random_case(500 + i, B, H, N, d, dtype="bf16", sigma=sigma)
+    _, _, v = gen.random_case(600 + i, B, H, N, d, dtype="bf16", v_dist="uniform")
+    qd, kd, vd = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    m = _slopes(ab, H, delta)
+    flags = sum(ABI[c] for c in combo) | (1 if mode.startswith("skip") else 0)
+    out, lse = ab.alibi_attn_fwd_ex(qd, kd, vd, causal=causal, flags=flags, clamp_min=cmin, softcap_z=z, slopes=m)
+    ab.alibi_check_error()
+    ro, rl, _ = oracle.attention(q.f32, k.f32, v.f32, m=None if m is None else m.astype(np.float64), causal=causal,
+                                 variant=sum(ORC[c] for c in combo), c_clamp=cmin, z_cap=z)
+    assert_bf16_out(host64(out), ro)
+    assert_close(host64(lse), rl, TOL_BF16_LSE, "lse")
+    if mode.startswith("skip"):
+        # leaving out tiles whose weights flush to zero changes no bit
+        o0, l0 = ab.alibi_attn_fwd_ex(qd, kd, vd, causal=True, slopes=m)
+        ab.alibi_check_error()
+        assert np.array_equal(host64(out), host64(o0)) and np.array_equal(host64(lse), host64(l0))
+
+
+def _bwd_cases(n=16, seed=20261203):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        causal = bool(rng.integers(2))
+        d = int(rng.choice([64, 128]))
+        N = _length(rng, 1100)
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        mode, combo, cmin, z, delta = _options(rng, causal, H, allow_skip=False)
+        out.append(pytest.param(i, causal, B, H, N, d, mode, combo, cmin, z, delta,
+                                id=f"{i:02d}-{'c' if causal else 'nc'}-B{B}H{H}N{N}d{d}-{mode}{'+'.join(combo)}"))
+    return out
+
+
+@pytest.mark.parametrize("i,causal,B,H,N,d,mode,combo,cmin,z,delta", _bwd_cases())
+def test_backward_random_configurations(ab, i, causal, B, H, N, d, mode, combo, cmin, z, delta):
+    q, k, _ = gen.random_case(700 + i, B, H, N, d, dtype="bf16", sigma=2.0)
+    _, _, v = gen.random_case(800 + i, B, H, N, d, dtype="bf16")
+    do, _, _ = gen.random_case(900 + i, B, H, N, d, dtype="bf16")
+    qd, kd, vd, dod = (dev(t, "bf16") for t in (q, k, v, do))
+    m = _slopes(ab, H, delta)
+    kw = dict(flags=sum(ABI[c] for c in combo), clamp_min=cmin, softcap_z=z, slopes=m)
+    out, lse = ab.alibi_attn_fwd_ex(qd, kd, vd, causal=causal, **kw)
+    dq, dk, dv = ab.alibi_attn_bwd(qd, kd, vd, out, lse, dod, causal=causal, **kw)
+    ab.alibi_check_error()
+    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, m=None if m is None else m.astype(np.float64),
+                                            causal=causal, variant=sum(ORC[c] for c in combo), c_clamp=cmin, z_cap=z)
+    assert_grad(host64(dq), rq, TOL_BF16_REL, "dq", bf16=True)
+    assert_grad(host64(dk), rk, TOL_BF16_REL, "dk", bf16=True)
+    assert_grad(host64(dv), rv, TOL_BF16_REL, "dv", bf16=True)
+
+
+def _dec_cases(n=16, seed=20261204):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        d = int(rng.choice([16, 32, 64, 128]))
+        B, H = int(rng.integers(1, 5)), int(rng.integers(1, 49))
+        L = _length(rng, max(1, min(30000, 400000 // (B * H))))
+        skip = bool(rng.integers(2))
+        out.append(pytest.param(i, B, H, L, d, skip, id=f"{i:02d}-B{B}H{H}L{L}d{d}{'-skip' if skip else ''}"))
+    return out
+
+
+@pytest.mark.parametrize("i,B,H,L,d,skip", _dec_cases())
+def test_decode_random_configurations(ab, i, B, H, L, d, skip):
+    w = gen.Workload("fz", "decode", B, H, L, d, "bf16", seed=1000 + i)
+    q, k, v = gen.generate(w)
+    qd, kd, vd = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    out = ab.alibi_attn_decode(qd, kd, vd)
+    if skip:
+        kn = ab.alibi_kv_block_norms(kd)
+        out_s = ab.alibi_attn_decode_skip(qd, kd, vd, kn)
+    ab.alibi_check_error()
+    ro, _ = oracle.decode(q.f32, k.f32, v.f32)
+    assert_bf16_out(host64(out), ro)
+    if skip:
+        assert_bf16_out(host64(out_s), ro, "out (skipping)")
+        # the omitted weights are below 2^-127 of the largest: agreement to bf16 rounding
+        assert np.abs(host64(out_s) - host64(out)).max() <= 2.0 ** -7
