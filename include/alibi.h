@@ -46,7 +46,7 @@ extern "C" {
 typedef enum {
     ALIBI_OK = 0,
     ALIBI_ERR_INVALID = -1,     /* null pointer, non-positive size, misaligned pointer */
-    ALIBI_ERR_UNSUPPORTED = -2, /* valid request this build does not implement (e.g. d) */
+    ALIBI_ERR_UNSUPPORTED = -2, /* valid request the library does not implement (e.g. d) */
     ALIBI_ERR_CUDA = -3,        /* a CUDA runtime/driver call or kernel launch failed    */
     ALIBI_ERR_TIMEOUT = -4      /* a bounded device-side wait expired (see alibi_check_error) */
 } alibi_status;
