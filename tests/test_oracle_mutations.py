@@ -31,6 +31,15 @@ MUTANTS = [
     ("logdist_no_plus1", "D = log(D + 1.0);", "D = log(D);"),
     ("clamp_min", "if ((variant & ORACLE_CLAMP) && B < c_clamp) B = c_clamp;",
      "if ((variant & ORACLE_CLAMP) && B > c_clamp) B = c_clamp;"),
+    ("noncausal_signed_distance", "double D = (double)(i >= j ? i - j : j - i);", "double D = (double)(i - j);"),
+    ("explicit_arithmetic_spacing", "double delta = delta_first * pow(delta_last / delta_first, t);",
+     "double delta = delta_first + (delta_last - delta_first) * t;"),
+    ("explicit_log_ignored", "double dist = log_distance ? log(delta + 1.0) : delta;", "double dist = delta;"),
+    ("prefill_one_slope", "const double m = c->m[h];", "const double m = c->m[0];"),
+    ("decode_one_slope", "x[j] = a - c->m[h] * (double)(pos - j);", "x[j] = a - c->m[0] * (double)(pos - j);"),
+    ("underflow_one_slope", "- c->m[h] * (double)(i - j);", "- c->m[0] * (double)(i - j);"),
+    ("weights_unnormalised", "double wij = x[j] / Z;", "double wij = x[j];"),
+    ("decode_unnormalised", "o[t] += (x[j] / Z) * (double)V", "o[t] += x[j] * (double)V"),
     # backward pass
     ("bwd_dq_no_rowdot", "double da = w * (bwd_g(c, bh, i, j) - c->rowdot[r]) * bwd_cap_factor(c, a);",
      "double da = w * bwd_g(c, bh, i, j) * bwd_cap_factor(c, a);"),
@@ -47,13 +56,16 @@ MUTANTS = [
 
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_reject_mutant(tmp_path, name, old, new):
+def test_pins_reject_mutant(name, old, new):
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation site for {name} not unique"
-    mut_c = tmp_path / f"{name}.c"
-    mut_c.write_text(src.replace(old, new))
-    mut_so = tmp_path / f"{name}.so"
-    oracle.compile_to(str(mut_c), str(mut_so))
+    work = os.path.join(os.path.dirname(SRC), "_build", "mutants")  # git-ignored build folder
+    os.makedirs(work, exist_ok=True)
+    mut_c = os.path.join(work, f"{name}.c")
+    with open(mut_c, "w") as f:
+        f.write(src.replace(old, new))
+    mut_so = os.path.join(work, f"{name}.so")
+    oracle.compile_to(mut_c, mut_so)
     env = dict(os.environ, ALIBI_ORACLE_LIB=str(mut_so))
     pins = "test_oracle_bwd_pins.py" if name.startswith("bwd_") else "test_oracle_pins.py"
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
