@@ -14,8 +14,10 @@
 // before using them, keeping ~8 KB per warp in flight at every d. One CTA per
 // (b, h) and split (one-dimensional grid, splits of a head adjacent); each CTA (8 warps) streams a contiguous slice of the cache,
 // merges its warps' partial softmaxes in shared memory, and either writes the
-// output (one split) or an fp32 partial (m, l, o[d]) that a second kernel
-// merges.
+// output (one split) or an fp32 partial (m, l, o[d]). With several splits, the
+// CTA that finishes a (b, h) last (a per-(b, h) counter it increments after a
+// device-wide fence) merges that head's partials and writes its output, so no
+// CTA ever waits for another and no second kernel is launched.
 //
 // Skipping ("When Attention Goes Blind" sec. 3.2-3.3 and 5.2: past its blindness
 // distance a head's weights are exactly zero): with per-64-key-block maximum key
@@ -46,6 +48,7 @@ struct DecodeParams {
     const __nv_bfloat16 *q, *k, *v;
     __nv_bfloat16 *out;
     float *part;  // [BH][splits][kPartStride], used when splits > 1
+    unsigned *count;  // [BH] splits finished per (b, h), zero between calls; used when splits > 1
     const float *knorm;  // optional [BH][nblk] max key norm per 64-key block: enables skipping
     int H, L, splits, chunk, nblk;
     float c1;  // log2(e) / sqrt(d)
@@ -69,6 +72,51 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
         f[2 * t] = __uint_as_float(w[t] << 16);
         f[2 * t + 1] = __uint_as_float(w[t] & 0xFFFF0000u);
     }
+}
+
+// One warp merges the splits' partial softmaxes of one (b, h) (lane t covers
+// o[4t .. 4t + 3]); the partials are read through L2 (written by other CTAs).
+template <int D>
+__device__ __forceinline__ void merge_partials(const float *base, int splits, __nv_bfloat16 *out_row, int lane)
+{
+    constexpr int kStride = DecCfg<D>::kPartStride;
+    float M = -INFINITY;
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, __ldcg(base + s * kStride));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    // lanes own 4 output columns each; the partials of 8 splits are loaded together
+    const bool mine = 4 * lane < D;
+    float Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+        float ms[8], ls[8];
+        float4 ov[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool in = s0 + j < splits;
+            const float *ps = base + (in ? s0 + j : 0) * kStride;
+            ms[j] = in ? __ldcg(ps) : -INFINITY;
+            ls[j] = in ? __ldcg(ps + 1) : 0.f;
+            ov[j] = (in && mine) ? __ldcg(reinterpret_cast<const float4 *>(ps + 4 + 4 * lane))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float a = (ms[j] == -INFINITY) ? 0.f : ex2_approx(ms[j] - M);
+            Lsum = fmaf(ls[j], a, Lsum);
+            O[0] = fmaf(ov[j].x, a, O[0]);
+            O[1] = fmaf(ov[j].y, a, O[1]);
+            O[2] = fmaf(ov[j].z, a, O[2]);
+            O[3] = fmaf(ov[j].w, a, O[3]);
+        }
+    }
+    if (!mine) return;
+    const float inv = 1.0f / Lsum;
+    __nv_bfloat162 r0 = __floats2bfloat162_rn(O[0] * inv, O[1] * inv);
+    __nv_bfloat162 r1 = __floats2bfloat162_rn(O[2] * inv, O[3] * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&r0);
+    pk.y = *reinterpret_cast<uint32_t *>(&r1);
+    *reinterpret_cast<uint2 *>(out_row + 4 * lane) = pk;
 }
 
 template <int D>
@@ -235,53 +283,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_kernel(const __grid_con
             dst[4 + t] = O;
         }
     }
-}
-
-// One warp per (b, h): merge the splits' partial softmaxes (lane t covers o[4t .. 4t + 3]).
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restrict__ part,
-                                                           __nv_bfloat16 *__restrict__ out, int BH, int splits)
-{
-    constexpr int kStride = DecCfg<D>::kPartStride;
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= BH) return;
-    const float *base = part + static_cast<size_t>(warp) * splits * kStride;
-    float M = -INFINITY;
-    for (int s = lane; s < splits; s += 32) M = fmaxf(M, base[s * kStride]);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    // lanes own 4 output columns each; the partials of 8 splits are loaded together
-    const bool mine = 4 * lane < D;
-    float Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s0 = 0; s0 < splits; s0 += 8) {
-        float ms[8], ls[8];
-        float4 ov[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const bool in = s0 + j < splits;
-            const float *ps = base + (in ? s0 + j : 0) * kStride;
-            ms[j] = in ? ps[0] : -INFINITY;
-            ls[j] = in ? ps[1] : 0.f;
-            ov[j] = (in && mine) ? *reinterpret_cast<const float4 *>(ps + 4 + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float a = (ms[j] == -INFINITY) ? 0.f : ex2_approx(ms[j] - M);
-            Lsum = fmaf(ls[j], a, Lsum);
-            O[0] = fmaf(ov[j].x, a, O[0]);
-            O[1] = fmaf(ov[j].y, a, O[1]);
-            O[2] = fmaf(ov[j].z, a, O[2]);
-            O[3] = fmaf(ov[j].w, a, O[3]);
-        }
-    }
-    if (!mine) return;
-    const float inv = 1.0f / Lsum;
-    __nv_bfloat162 r0 = __floats2bfloat162_rn(O[0] * inv, O[1] * inv);
-    __nv_bfloat162 r1 = __floats2bfloat162_rn(O[2] * inv, O[3] * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t *>(&r0);
-    pk.y = *reinterpret_cast<uint32_t *>(&r1);
-    *reinterpret_cast<uint2 *>(out + static_cast<size_t>(warp) * D + 4 * lane) = pk;
+    if (p.splits == 1) return;
+    // Count this split as done once its partial is visible device-wide; the CTA that
+    // counts a (b, h) last merges it (no CTA waits for another) and re-arms the counter.
+    __shared__ bool last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(p.count + bh, 1u) == static_cast<unsigned>(p.splits - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();  // the other splits' partials, counted before this CTA, are read after it
+    if (warp == 0)
+        merge_partials<D>(p.part + static_cast<size_t>(bh) * p.splits * C::kPartStride, p.splits,
+                          p.out + static_cast<size_t>(bh) * D, lane);
+    if (threadIdx.x == 0) p.count[bh] = 0u;  // zero again for the next call that uses this buffer
 }
 
 // Maximum key norm of each 64-key block of the cache: one CTA per (b, h) and block
@@ -346,8 +361,6 @@ cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, in
     return cudaGetLastError();
 }
 
-// Split count: enough CTAs for several waves (two resident per SM), at least
-// 512 keys per split, and every split non-empty.
 // Split count: with eight or more waves of whole heads (two resident CTAs per SM)
 // every SM streams whole heads and there is nothing to merge; with fewer, each
 // head's cache is cut into the number of slices that minimises (waves of CTAs) x
@@ -362,7 +375,7 @@ int decode_splits(int BH, int L)
     long long best_cost = -1;
     for (int s = 1; s <= max_s && s <= 4096; ++s) {
         const long long waves = (static_cast<long long>(BH) * s + R - 1) / R;
-        // a split also costs its merge: a second launch and the partials (~512 keys)
+        // a split also costs its merge: the partials and the merging CTA's pass (~512 keys)
         const long long cost = waves * ((L + s - 1) / s + 256) + (s > 1 ? 512 : 0);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
@@ -377,11 +390,14 @@ size_t decode_partials_bytes(int BH, int splits, int d)
     return splits > 1 ? static_cast<size_t>(BH) * splits * (d + 4) * sizeof(float) : 0;
 }
 
+size_t decode_counters_bytes(int BH, int splits) { return splits > 1 ? static_cast<size_t>(BH) * sizeof(unsigned) : 0; }
+
 bool decode_supports(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 template <int D>
 static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B,
-                                   int H, int L, const Slopes &slopes, int splits, float *partials, cudaStream_t stream)
+                                   int H, int L, const Slopes &slopes, int splits, float *partials, unsigned *counters,
+                                   cudaStream_t stream)
 {
     using C = DecCfg<D>;
     DecodeParams p;
@@ -390,6 +406,7 @@ static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc
     p.v = static_cast<const __nv_bfloat16 *>(vc);
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.part = partials;
+    p.count = counters;
     p.H = H;
     p.L = L;
     p.splits = splits;
@@ -406,22 +423,24 @@ static cudaError_t launch_decode_d(const void *q, const void *kc, const void *vc
     const long long nblocks = static_cast<long long>(p.splits) * BH;
     if (nblocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>(nblocks);
+    if (p.splits > 1 && (!partials || !counters)) return cudaErrorInvalidValue;
     decode_kernel<D><<<grid, kWarps * 32, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || p.splits == 1) return e;
-    decode_merge_kernel<D><<<(BH + 3) / 4, 128, 0, stream>>>(partials, p.out, BH, p.splits);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B,
                                int H, int L, int d, const Slopes &slopes, int splits, float *partials,
-                               cudaStream_t stream)
+                               unsigned *counters, cudaStream_t stream)
 {
     switch (d) {
-        case 128: return launch_decode_d<128>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
-        case 64: return launch_decode_d<64>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
-        case 32: return launch_decode_d<32>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
-        case 16: return launch_decode_d<16>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, stream);
+        case 128:
+            return launch_decode_d<128>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, counters, stream);
+        case 64:
+            return launch_decode_d<64>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, counters, stream);
+        case 32:
+            return launch_decode_d<32>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, counters, stream);
+        case 16:
+            return launch_decode_d<16>(q, kc, vc, knorm, out, B, H, L, slopes, splits, partials, counters, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -432,11 +451,19 @@ cudaError_t launch_decode(const void *q, const void *kc, const void *vc, const f
     if (!decode_supports(d)) return cudaErrorInvalidValue;
     const int BH = B * H;
     const int splits = decode_splits(BH, L);
-    if (splits == 1) return launch_decode_with(q, kc, vc, knorm, out, B, H, L, d, slopes, 1, nullptr, stream);
+    if (splits == 1)
+        return launch_decode_with(q, kc, vc, knorm, out, B, H, L, d, slopes, 1, nullptr, nullptr, stream);
+    // partials, then the per-(b, h) counters (zeroed here: pool memory holds whatever its last user left)
+    const size_t pb = (decode_partials_bytes(BH, splits, d) + 255) & ~size_t(255);
+    const size_t cb = decode_counters_bytes(BH, splits);
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, decode_partials_bytes(BH, splits, d), decode_pool(), stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, pb + cb, decode_pool(), stream);
     if (e != cudaSuccess) return e;
-    e = launch_decode_with(q, kc, vc, knorm, out, B, H, L, d, slopes, splits, static_cast<float *>(ws), stream);
+    unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + pb);
+    e = cudaMemsetAsync(counters, 0, cb, stream);
+    if (e == cudaSuccess)
+        e = launch_decode_with(q, kc, vc, knorm, out, B, H, L, d, slopes, splits, static_cast<float *>(ws), counters,
+                               stream);
     cudaError_t f = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : f;
 }

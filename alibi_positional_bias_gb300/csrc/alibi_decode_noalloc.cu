@@ -22,15 +22,21 @@ namespace {
 // library holds it until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+// Per-(b, h) split counters: zero when the library loads, and every call leaves
+// them zero again (the CTA that merges a (b, h) resets its counter). 4 MiB of
+// partials hold at most 26214 (b, h) pairs with two or more splits.
+constexpr int kNoAllocCounters = 32768;
+static __device__ unsigned g_noalloc_counters[kNoAllocCounters];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 float *g_scratch_addr[kMaxDevices] = {};
+unsigned *g_counters_addr[kMaxDevices] = {};
 
 // One-time set-up per device, with that device current: in host code the
 // array's name is only a host-side stand-in, so the kernel must be given the
 // device address the runtime reports for it.
-cudaError_t scratch_address(float **addr)
+cudaError_t scratch_address(float **addr, unsigned **counters)
 {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -38,12 +44,16 @@ cudaError_t scratch_address(float **addr)
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> g(g_mu);
     if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
+        void *p = nullptr, *c = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
+        e = cudaGetSymbolAddress(&c, g_noalloc_counters);
+        if (e != cudaSuccess) return e;
+        g_counters_addr[dev] = static_cast<unsigned *>(c);
         g_scratch_addr[dev] = static_cast<float *>(p);
     }
     *addr = g_scratch_addr[dev];
+    *counters = g_counters_addr[dev];
     return cudaSuccess;
 }
 
@@ -66,13 +76,17 @@ extern "C" int alibi_attn_decode_noalloc(const void *q, const void *kcache, cons
     // same split plan as alibi_attn_decode, so both give the same result
     const int splits = decode_splits(B * H, L);
     if (decode_partials_bytes(B * H, splits, d) > kNoAllocScratchBytes) return ALIBI_ERR_UNSUPPORTED;
+    if (splits > 1 && B * H > kNoAllocCounters) return ALIBI_ERR_UNSUPPORTED;
     float *scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess) return ALIBI_ERR_CUDA;
+    unsigned *counters = nullptr;
+    if (scratch_address(&scratch, &counters) != cudaSuccess) return ALIBI_ERR_CUDA;
     Slopes s;
     fill_slopes(H, &s);
     // Every partial the merge reads is written earlier in the same call, so the
     // buffer needs no clearing; what the previous call left there is overwritten.
+    // The counters are zero between calls (each call's merging CTAs reset theirs).
     const cudaError_t e = launch_decode_with(q, kcache, vcache, nullptr, out, B, H, L, d, s, splits,
-                                             splits > 1 ? scratch : nullptr, static_cast<cudaStream_t>(stream));
+                                             splits > 1 ? scratch : nullptr, splits > 1 ? counters : nullptr,
+                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ALIBI_OK : ALIBI_ERR_CUDA;
 }

@@ -39,12 +39,15 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint
 int decode_splits(int BH, int L);
 // Bytes of split-K partials the decode needs for that plan (0 when it does not split).
 size_t decode_partials_bytes(int BH, int splits, int d);
+// Bytes of per-(b, h) split counters for that plan (0 when it does not split).
+size_t decode_counters_bytes(int BH, int splits);
 // Head sizes the decode kernels are built for (16, 32, 64, 128).
 bool decode_supports(int d);
-// Launch the decode kernels with a caller-provided partials buffer (used when splits > 1).
+// Launch the decode kernel with caller-provided partials and counters (used when
+// splits > 1). The counters must be zero at launch; the kernel leaves them zero.
 cudaError_t launch_decode_with(const void *q, const void *kc, const void *vc, const float *knorm, void *out, int B,
                                int H, int L, int d, const Slopes &slopes, int splits, float *partials,
-                               cudaStream_t stream);
+                               unsigned *counters, cudaStream_t stream);
 // Maximum key norm per 64-key block, blocks [blk_begin, ceil(L/64)) of every (b, h).
 cudaError_t launch_kv_block_norms(const void *kc, float *knorm, int B, int H, int L, int d, int blk_begin,
                                   cudaStream_t stream);

@@ -501,9 +501,12 @@ def run_native(args):
         with torch.cuda.graph(graph, stream=gs):
             ab.alibi_attn_decode(*s1, out=o1)
         t_graph = timed_ms(lambda: graph.replay())
+        # the allocation-free entry point: no pool allocation and no counter memset per call
+        t_noalloc = timed_ms(lambda: ab.alibi_attn_decode_noalloc(*s1, o1, stream=stream))
         single = {"shape": f"B=1 H={wd.H} L={wd.N} d={wd.d}", "splits": ab.alibi_attn_decode_splits(1, wd.H, wd.N, wd.d),
-                  "us_direct": 1e3 * t_direct, "us_graph": 1e3 * t_graph,
-                  "gbs_graph": decode_bytes(w1) / (t_graph / 1e3) / 1e9}
+                  "us_direct": 1e3 * t_direct, "us_graph": 1e3 * t_graph, "us_noalloc_direct": 1e3 * t_noalloc,
+                  "gbs_graph": decode_bytes(w1) / (t_graph / 1e3) / 1e9,
+                  "gbs_noalloc_direct": decode_bytes(w1) / (t_noalloc / 1e3) / 1e9}
         del s1, o1, graph
 
     # ------------------------------------------------ end to end (host buffers)

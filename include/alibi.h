@@ -198,9 +198,11 @@ ALIBI_API int alibi_attn_fwd_f32(const float *q, const float *k, const float *v,
  * Biases", KV-cache paragraph): s_j = q.k_j/sqrt(d) - m_h (L - 1 - j).
  * q: device bf16 [B, H, d]; kcache, vcache: device bf16 [B, H, L, d];
  * out: device bf16 [B, H, d]. d in {16, 32, 64, 128}; L >= 1.
- * Split-K over the cache with an fp32 partial-softmax merge. When it splits,
- * the partials buffer is taken from a library-owned stream-ordered memory pool
- * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).
+ * Split-K over the cache with an fp32 partial-softmax merge, done in the same
+ * kernel by the CTA that finishes each (b, h) last. When it splits, the
+ * partials buffer and B*H split counters are taken from a library-owned
+ * stream-ordered memory pool (cudaMallocFromPoolAsync / cudaFreeAsync on
+ * `stream`) and the counters are zeroed with cudaMemsetAsync on `stream`.
  */
 ALIBI_API int alibi_attn_decode(const void *q, const void *kcache, const void *vcache, void *out,
                       int B, int H, int L, int d, void *stream);
@@ -234,8 +236,9 @@ ALIBI_API int alibi_attn_decode_skip(const void *q, const void *kcache, const vo
 /*
  * Number of KV-cache splits alibi_attn_decode uses for this shape (host-only,
  * deterministic for a given device). 1 means a single kernel with no partials
- * buffer; S > 1 means a split kernel plus a merge kernel and a partials buffer
- * of B*H*S*(d+4) floats. Returns a negative alibi_status on invalid arguments.
+ * buffer; S > 1 means one kernel of S CTAs per (b, h) whose last CTA merges,
+ * with a partials buffer of B*H*S*(d+4) floats and B*H counters. Returns a
+ * negative alibi_status on invalid arguments.
  */
 ALIBI_API int alibi_attn_decode_splits(int B, int H, int L, int d);
 
@@ -246,16 +249,19 @@ ALIBI_API int alibi_attn_decode_splits(int B, int H, int L, int d);
  * real-time decode loop that cannot absorb allocation latency, a runtime that
  * forbids allocations outside its own arena). Same arguments, layouts, split
  * plan and results as alibi_attn_decode; the caller still passes inputs and
- * outputs. The split-K partials live in a fixed 4 MiB device buffer compiled
- * into the library (held by every GPU that loads it until process exit); no
- * cudaMalloc, cudaFree or pool allocation happens.
+ * outputs. The split-K partials live in a fixed 4 MiB device buffer and the
+ * split counters in a fixed 128 KiB one, both compiled into the library (held
+ * by every GPU that loads it until process exit); no cudaMalloc, cudaFree, pool
+ * allocation or memset happens.
  *   - The first call on each device does a one-time set-up (it looks up the
  *     buffer's device address); make that first call before any stream capture.
  *   - All calls share the buffer and it keeps the last call's contents (each
- *     call overwrites every partial it reads, so nothing needs clearing). Calls
- *     that overlap on the GPU (e.g. on different streams) race on it: order them.
+ *     call overwrites every partial it reads, so nothing needs clearing, and
+ *     leaves every counter at zero, as the library loads them). Calls that
+ *     overlap on the GPU (e.g. on different streams) race on it: order them.
  *   - Returns ALIBI_ERR_UNSUPPORTED if the split plan needs more than 4 MiB of
- *     partials (B*H*S*(d+4)*4 bytes with S = alibi_attn_decode_splits(...)).
+ *     partials (B*H*S*(d+4)*4 bytes with S = alibi_attn_decode_splits(...)) or
+ *     more than 32768 (b, h) pairs split.
  */
 ALIBI_API int alibi_attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, void *out,
                       int B, int H, int L, int d, void *stream);

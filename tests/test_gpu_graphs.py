@@ -15,7 +15,7 @@ def ab():
     return ab
 
 
-@pytest.mark.parametrize("B,H,L", [(1, 40, 8192), (64, 8, 1024)])  # split (merge launch) and single pass
+@pytest.mark.parametrize("B,H,L", [(1, 40, 8192), (64, 8, 1024)])  # split (counters, merging CTA) and single pass
 def test_decode_graph_replay(ab, B, H, L):
     import torch
     w = gen.Workload("dec", "decode", B, H, L, 128, "bf16", seed=5)
