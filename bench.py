@@ -47,8 +47,13 @@ def parse_args():
     # profiling helpers: run one kernel family on a reduced instance of its workload
     ap.add_argument("--only", choices=["prefill", "decode", "decode_skip", "backward"], default=None)
     ap.add_argument("--prefill-heads", type=int, default=None, help="override H of the prefill workload")
+    ap.add_argument("--prefill-workload", choices=["long_n16384", "layer_n2048", "heads6_n1024"], default=None,
+                    help="prefill workload of a profiling run (with --only prefill or backward)")
     ap.add_argument("--decode-batch", type=int, default=None, help="override B of the decode workload")
-    return ap.parse_args()
+    a = ap.parse_args()
+    if a.prefill_workload and a.only not in ("prefill", "backward"):
+        ap.error("--prefill-workload is for profiling runs (--only prefill or backward)")
+    return a
 
 
 def load_peaks():
@@ -238,7 +243,7 @@ def run_native(args):
 
     ab.load(build_if_missing=True)
     peaks = load_peaks()
-    wp, wd = gen.WORKLOADS[PREFILL], gen.WORKLOADS[DECODE]
+    wp, wd = gen.WORKLOADS[args.prefill_workload or PREFILL], gen.WORKLOADS[DECODE]
     if args.prefill_heads:
         wp = gen.Workload(**{**wp.__dict__, "H": args.prefill_heads})
     if args.decode_batch:
@@ -273,7 +278,7 @@ def run_native(args):
         dout = torch.empty_like(dq)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     splits = ab.alibi_attn_decode_splits(wd.B, wd.H, wd.N, wd.d)
-    launches_per_step = int(do_pre) + (2 if splits > 1 else 1) * int(do_dec)
+    launches_per_step = int(do_pre) + int(do_dec)  # a split decode merges in the same kernel
     stream = torch.cuda.current_stream(dev)
 
     if args.only == "backward":  # profiling run: the backward kernels alone
