@@ -26,7 +26,13 @@ MUTANTS = [
     ("lse_without_max", "if (c->lse) c->lse[r] = M + log(Z);", "if (c->lse) c->lse[r] = log(Z);"),
     ("decode_position", "const long pos = (long)c->L - 1;", "const long pos = (long)c->L;"),
     ("underflow_no_max", "double e = x[j] - M;", "double e = x[j];"),
-    ("threshold_127", "t[2] = -126.0 * ln2;", "t[2] = -127.0 * ln2;"),
+    ("underflow_strict", "if (e <= c->tau) ++cnt;", "if (e < c->tau) ++cnt;"),
+    ("band_strict", "if (fabs(e - c->tau) <= c->band) ++nr;", "if (fabs(e - c->tau) < c->band) ++nr;"),
+    ("band_around_zero", "if (fabs(e - c->tau) <= c->band) ++nr;", "if (fabs(e) <= c->band) ++nr;"),
+    ("band_in_log2_units", "if (fabs(e - c->tau) <= c->band) ++nr;",
+     "if (fabs(e - c->tau) <= c->band * 0.6931471805599453) ++nr;"),
+    ("band_below_only", "if (fabs(e - c->tau) <= c->band) ++nr;", "if (e - c->tau <= c->band) ++nr;"),
+    ("threshold_127","t[2] = -126.0 * ln2;", "t[2] = -127.0 * ln2;"),
     ("softcap_no_z", "return z * tanh(a / z);", "return tanh(a / z);"),
     ("logdist_no_plus1", "D = log(D + 1.0);", "D = log(D);"),
     ("clamp_min", "if ((variant & ORACLE_CLAMP) && B < c_clamp) B = c_clamp;",

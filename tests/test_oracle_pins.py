@@ -338,6 +338,33 @@ def test_underflow_counter_closed_form():
         assert cnt[h] == want, h
 
 
+@pytest.mark.parametrize("band", [0.0, 1.25, 3.65])
+def test_underflow_band_closed_form(band):
+    # The counter's second output is the number of entries whose max-subtracted
+    # exponent lies within +-band of tau: the entries whose side of the "<= tau"
+    # crossing ("When Attention Goes Blind", sec. 3.2) depends on rounding. With
+    # Q = 0 row i's exponent at distance D is exactly -m D (the diagonal holds
+    # the max), so per head the count is the sum of (N - D) over the distances
+    # D < N with |-m D - tau| <= band, evaluated here in exact rationals. tau is
+    # chosen so that -m D = tau exactly for the dyadic slopes (ties at band 0
+    # and at both edges of band 1.25 count), and 0.3 has no tie.
+    from fractions import Fraction
+    N, tau = 300, -25.0
+    m = np.array([0.25, 0.5, 0.0625, 0.3, 0.125])
+    q = np.zeros((1, m.size, N, 4), np.float32)
+    k = np.random.default_rng(1).standard_normal(q.shape).astype(np.float32)
+    cnt, near = oracle.underflow_counts_per_head(q, k, tau, m=m, band=band)
+    for h, mh in enumerate(m):
+        fm, ft, fb = Fraction(float(mh)), Fraction(tau), Fraction(band)
+        want_near = sum(N - D for D in range(N) if abs(-fm * D - ft) <= fb)
+        want_cnt = sum(N - D for D in range(N) if -fm * D <= ft)
+        assert near[h] == want_near, (h, band)
+        assert cnt[h] == want_cnt, h
+    # the tie at band 0: slope 0.25 reaches -25 at D = 100 exactly
+    if band == 0.0:
+        assert near[0] == N - 100 and near[1] == N - 50 and near[3] == 0
+
+
 def test_fraction_36_6_percent():
     # sec. 3.3 / Fig. 1b: at a token distance of 2048, 36.6% of the entries of a
     # 16-head bf16 layer have underflowed (A = 0). Reading: the last row of a
