@@ -23,6 +23,7 @@ __all__ = [
     "AlibiError", "load", "lib_path", "exported_symbols", "alibi_version", "alibi_status_str", "alibi_slopes",
     "alibi_attn_fwd", "alibi_attn_fwd_ex", "alibi_attn_skip_plan", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits", "alibi_attn_probs_f32",
     "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_attn_decode_noalloc", "alibi_selftest_timeout",
+    "alibi_selftest_fwd_timeout", "alibi_decode_underflow_bf16",
     "alibi_slopes_explicit", "alibi_attn_probs_f32_ex", "AlibiFwdOptions", "alibi_attn_bwd", "alibi_attn_bwd_f32",
     "alibi_kv_block_norms", "alibi_attn_decode_skip",
 ]
@@ -90,6 +91,10 @@ def load(build_if_missing: bool = False):
         lib.alibi_check_error.argtypes = [vp]
         lib.alibi_selftest_timeout.argtypes = [vp]
         lib.alibi_selftest_timeout.restype = I
+        lib.alibi_selftest_fwd_timeout.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, vp]
+        lib.alibi_selftest_fwd_timeout.restype = I
+        lib.alibi_decode_underflow_bf16.argtypes = [vp, vp, I, I, I, I, F, vp, vp]
+        lib.alibi_decode_underflow_bf16.restype = I
         for name in ("alibi_attn_fwd", "alibi_attn_fwd_f32", "alibi_attn_decode", "alibi_attn_decode_splits",
                      "alibi_attn_probs_f32",
                      "alibi_attn_underflow_bf16", "alibi_check_error", "alibi_slopes"):
@@ -418,10 +423,43 @@ def alibi_attn_underflow_bf16(q, k, tau: float, counts=None, stream=None):
     return counts
 
 
+def alibi_decode_underflow_bf16(q, kcache, tau: float, counts=None, stream=None):
+    """Per-head counts of cached keys whose max-subtracted exponent at the decode row is <= tau."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, d = q.shape
+    _need(kcache, torch.bfloat16, None, "kcache")
+    if kcache.dim() != 4 or tuple(kcache.shape[:2]) != (B, H) or kcache.shape[3] != d:
+        raise ValueError("kcache must be [B, H, L, d] matching q [B, H, d]")
+    L = kcache.shape[2]
+    if counts is None:
+        counts = torch.empty((H,), dtype=torch.int64, device=q.device)
+    _need(counts, torch.int64, (H,), "counts")
+    _check(load().alibi_decode_underflow_bf16(_ptr(q), _ptr(kcache), B, H, L, d, ctypes.c_float(tau), _ptr(counts),
+                                              _stream(stream, q.device)), "alibi_decode_underflow_bf16")
+    return counts
+
+
 def alibi_selftest_timeout(stream=None) -> None:
     """Launch the failure-path self-test (a bounded wait that must time out)."""
     import torch
     _check(load().alibi_selftest_timeout(_stream(stream, torch.cuda.current_device())), "alibi_selftest_timeout")
+
+
+def alibi_selftest_fwd_timeout(q, k, v, wait_us: int = 20000, out=None, lse=None, stream=None):
+    """Run the prefill kernel with one Q load left out and a short wait limit (failure-path self-test)."""
+    import torch
+    _need(q, torch.bfloat16, None, "q")
+    B, H, N, d = q.shape
+    _need(k, torch.bfloat16, q.shape, "k")
+    _need(v, torch.bfloat16, q.shape, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(load().alibi_selftest_fwd_timeout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                             int(wait_us), _stream(stream, q.device)), "alibi_selftest_fwd_timeout")
+    return out, lse
 
 
 def alibi_check_error(stream=None, device=None) -> None:

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     uint32_t *err = p.err;
 
     if (threadIdx.x == 0) {
+        cta_err_init(kWaitLimitNs);
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
         for (int s = 0; s < 2; ++s) {
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------ TMA producer
             uint32_t qc = 0;
+            int kres = -1;  // item whose resident K, V were issued last
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 const BItem t = dkdv_item(p, w, CAUSAL);
                 ok = mbar_wait(kv_empty, (k & 1) ^ 1, err, SITE_B_PROD_RES);
                 if (!ok) break;
+                kres = k;
                 mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
                     tma_load_3d(smem + C::kRes0 + c * C::kChunkBytes, &p.tk, 64 * c, t.tile * BT, t.bh, kv_full);
@@ -326,6 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                     }
                 }
             }
+            // Drain (also after an error): the last resident load and the last load into
+            // each ring stage have landed before the CTA can exit.
+            if (kres >= 0) mbar_wait(kv_full, kres & 1, err, SITE_B_PROD_RES, true);
+            for (uint32_t n = qc > 2 ? qc - 2 : 0; n < qc; ++n)
+                mbar_wait(&qo_full[n & 1], (n >> 1) & 1, err, SITE_B_PROD_RING, true);
         } else if (warp == 1) {
             // whole warp, converged; one elected lane issues each tcgen05 instruction
             // -------------------------------------------------------- MMA issuer
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 mma_commit_w(acc_full);
             }
             mma_commit_w(mma_done);
-            mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE);
+            mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE, true);
         }
     } else {
         // --------------------------------------------------- elementwise warps
@@ -628,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     uint32_t *err = p.err;
 
     if (threadIdx.x == 0) {
+        cta_err_init(kWaitLimitNs);
         mbar_init(qd_full, 1);
         mbar_init(qd_empty, 1);
         for (int s = 0; s < 2; ++s) {
@@ -666,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
         if (warp == 0 && lane == 0) {
             uint32_t kc = 0;
+            int kres = -1;  // item whose resident Q, dO were issued last
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
@@ -673,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 const BItem t = dq_item(p, w, CAUSAL);
                 ok = mbar_wait(qd_empty, (k & 1) ^ 1, err, SITE_B_PROD_RES);
                 if (!ok) break;
+                kres = k;
                 mbar_arrive_expect_tx(qd_full, 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
                     tma_load_3d(smem + C::kRes0 + c * C::kChunkBytes, &p.tq, 64 * c, t.tile * BT, t.bh, qd_full);
@@ -691,6 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                     }
                 }
             }
+            // Drain (also after an error), as in the dK/dV kernel.
+            if (kres >= 0) mbar_wait(qd_full, kres & 1, err, SITE_B_PROD_RES, true);
+            for (uint32_t n = kc > 2 ? kc - 2 : 0; n < kc; ++n)
+                mbar_wait(&kv_full[n & 1], (n >> 1) & 1, err, SITE_B_PROD_RING, true);
         } else if (warp == 1) {
             // whole warp, converged; one elected lane issues each tcgen05 instruction
             // S and dP in two halves of 64 keys (the columns of one elementwise warpgroup
@@ -782,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 mma_commit_w(acc_full);
             }
             mma_commit_w(mma_done);
-            mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE);
+            mbar_wait(mma_done, 0, err, SITE_B_MMA_DONE, true);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
@@ -964,18 +979,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
     if (row < rows && l == 0) dsum[row] = acc;
 }
 
-template <typename K>
-cudaError_t check_launch_regs(K kernel, uint32_t smem)
-{
-    // The register split only balances if the kernel launches with exactly kLaunchRegs per
-    // thread; refuse to launch otherwise (an unbalanced setmaxnreg.inc would never return).
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-}
-
 template <int D, bool VAR>
 cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void *out, const float *lse,
                          const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int causal,
@@ -983,14 +986,17 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
                          cudaStream_t stream)
 {
     using C = BwdCfg<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = check_launch_regs(bwd_dkdv_kernel<D, VAR, true>, C::kSmem);
-        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D, VAR, true>, C::kSmem);
-        if (e == cudaSuccess) e = check_launch_regs(bwd_dkdv_kernel<D, VAR, false>, C::kSmem);
-        if (e == cudaSuccess) e = check_launch_regs(bwd_dq_kernel<D, VAR, false>, C::kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
+    // The register split only balances if the kernels launch with exactly kLaunchRegs per
+    // thread; prepare_kernel refuses otherwise (an unbalanced setmaxnreg.inc never returns).
+    {
+        const void *kerns[4] = {reinterpret_cast<const void *>(bwd_dkdv_kernel<D, VAR, true>),
+                                reinterpret_cast<const void *>(bwd_dq_kernel<D, VAR, true>),
+                                reinterpret_cast<const void *>(bwd_dkdv_kernel<D, VAR, false>),
+                                reinterpret_cast<const void *>(bwd_dq_kernel<D, VAR, false>)};
+        for (const void *kern : kerns) {
+            const cudaError_t e = prepare_kernel(kern, C::kSmem, kLaunchRegs);
+            if (e != cudaSuccess) return e;
+        }
     }
     const long long rows = static_cast<long long>(B) * H * N;
     constexpr int kRowsPerCta = 8 * (32 / (D / 8));

@@ -84,6 +84,8 @@ struct FwdParams {
     __nv_bfloat16 *out;
     float *lse;
     uint32_t *err;
+    uint64_t wait_ns;  // limit of every bounded wait
+    int test_skip_q0;  // failure-path self-test: the producer leaves out the first item's Q tile 0
     int N, BH, H, NQB, NQT, num_items;
     int dr;  // the tensors' head size (<= D: the D = 64 kernel also serves d = 16 and 32)
     int causal;  // 1: keys j <= i only; 0: every key, distance |i - j|
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     uint32_t *err = p.err;
 
     if (threadIdx.x == 0) {
+        cta_err_init(p.wait_ns);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&q_full[s], 1);
             mbar_init(&k_full[s], 1);
@@ -272,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t kc = 0, vc = 0;
+            int qk[2] = {-1, -1};  // item whose Q tile s was issued last
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
@@ -280,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 ok = mbar_wait(q_empty, (k & 1) ^ 1, err, SITE_PROD_Q);
                 if (!ok) break;
                 for (int s = 0; s < 2; ++s) {
+                    if (p.test_skip_q0 && k == 0 && s == 0) continue;
+                    qk[s] = k;
                     mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_3d(smem + C::kQ + s * C::kTileBytes + c * C::kChunkBytes, &p.tq, 64 * c,
@@ -304,6 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 }
                 if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, kv_tile(p, t, t.n - 1), SITE_PROD_V);
             }
+            // Drain (also after an error): the last load into each Q slot and ring stage
+            // has landed before the CTA can exit. Earlier loads into a stage were consumed,
+            // hence complete, before the stage was reused.
+            for (int s = 0; s < 2; ++s)
+                if (qk[s] >= 0) mbar_wait(&q_full[s], qk[s] & 1, err, SITE_PROD_Q, true);
+            for (uint32_t n = kc > 2 ? kc - 2 : 0; n < kc; ++n)
+                mbar_wait(&k_full[n % 2], (n / 2) & 1, err, SITE_PROD_K, true);
+            for (uint32_t n = vc > 2 ? vc - 2 : 0; n < vc; ++n)
+                mbar_wait(&v_full[n % 2], (n / 2) & 1, err, SITE_PROD_V, true);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             }
             // drain: every MMA issued above completes before TMEM is released
             mma_commit_w(mma_done);
-            mbar_wait(mma_done, 0, err, SITE_MMA_DONE);
+            mbar_wait(mma_done, 0, err, SITE_MMA_DONE, true);
         }
     }
     } else {
@@ -673,7 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 template <int D, bool VAR>
 static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                                    int H, int N, int dr, int causal, const Slopes &slopes, const int2 *plan,
-                                   unsigned int variant, float clamp_min, float softcap_z, cudaStream_t stream)
+                                   unsigned int variant, float clamp_min, float softcap_z, uint64_t test_wait_ns,
+                                   cudaStream_t stream)
 {
     using C = Cfg<D>;
     FwdParams p;
@@ -687,6 +703,8 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     p.lse = lse;
     p.err = device_status_word();
     if (!p.err) return cudaErrorInvalidDevice;
+    p.wait_ns = test_wait_ns ? test_wait_ns : kWaitLimitNs;
+    p.test_skip_q0 = test_wait_ns != 0;
     p.N = N;
     p.BH = static_cast<int>(BH);
     p.H = H;
@@ -702,21 +720,13 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     p.cap_k = (variant & kFwdSoftcap) ? 2.0f * 1.4426950408889634f / (sqrtf(static_cast<float>(dr)) * softcap_z) : 0.f;
     p.cap_zl = softcap_z * 1.4426950408889634f;
 
-    static bool attr_set = false;  // per process; the attribute is per function
-    if (!attr_set) {
-        // The register split above only balances if the kernel launches with exactly
-        // kLaunchRegs per thread; refuse to launch otherwise (an unbalanced
-        // setmaxnreg.inc would wait for registers that never come).
-        cudaFuncAttributes fa;
-        for (int c = 0; c < 2; ++c) {
-            const auto kern = c ? fwd_tc_kernel<D, VAR, true> : fwd_tc_kernel<D, VAR, false>;
-            cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-            if (e != cudaSuccess) return e;
-            if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-            if (e != cudaSuccess) return e;
-        }
-        attr_set = true;
+    // The register split above only balances if the kernel launches with exactly
+    // kLaunchRegs per thread; prepare_kernel refuses otherwise (an unbalanced
+    // setmaxnreg.inc would wait for registers that never come).
+    for (int c = 0; c < 2; ++c) {
+        const auto kern = c ? fwd_tc_kernel<D, VAR, true> : fwd_tc_kernel<D, VAR, false>;
+        const cudaError_t e = prepare_kernel(reinterpret_cast<const void *>(kern), C::kSmem, kLaunchRegs);
+        if (e != cudaSuccess) return e;
     }
     const int grid = p.num_items < num_sms() ? p.num_items : num_sms();
     if (causal)
@@ -728,20 +738,20 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
 
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
                           int d, int causal, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
-                          cudaStream_t stream)
+                          cudaStream_t stream, uint64_t test_wait_ns)
 {
     if (d != 128 && d != 64 && d != 32 && d != 16) return cudaErrorInvalidValue;
     auto run = [&](const int2 *plan) {
         const bool var = (flags & (kFwdClamp | kFwdLogDist | kFwdSoftcap)) != 0;
         if (d == 128)
             return var ? launch_fwd_tc_d<128, true>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags,
-                                                    clamp_min, softcap_z, stream)
+                                                    clamp_min, softcap_z, test_wait_ns, stream)
                        : launch_fwd_tc_d<128, false>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags,
-                                                     clamp_min, softcap_z, stream);
+                                                     clamp_min, softcap_z, test_wait_ns, stream);
         return var ? launch_fwd_tc_d<64, true>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags, clamp_min,
-                                               softcap_z, stream)
+                                               softcap_z, test_wait_ns, stream)
                    : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags, clamp_min,
-                                                softcap_z, stream);
+                                                softcap_z, test_wait_ns, stream);
     };
     if (!(flags & kFwdSkipUnderflow)) return run(nullptr);
     // underflow skipping: the plan lives in a stream-ordered scratch buffer for this call

@@ -108,6 +108,29 @@ int num_sms()
     return g_sms[dev];
 }
 
+cudaError_t prepare_kernel(const void *func, int smem, uint32_t regs)
+{
+    struct Prepared {
+        int dev;
+        const void *func;
+    };
+    static Prepared done[256];
+    static int ndone = 0;
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_mu);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].dev == dev && done[i].func == func) return cudaSuccess;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    if (regs != 0 && fa.numRegs != static_cast<int>(regs)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (ndone < 256) done[ndone++] = {dev, func};  // a full table only repeats the (idempotent) set-up
+    return cudaSuccess;
+}
+
 cudaMemPool_t decode_pool()
 {
     const int dev = current_device();
@@ -216,6 +239,8 @@ static int check_dims(int B, int H, int N, int d)
     if (H > kMaxHeads) return ALIBI_ERR_UNSUPPORTED;
     // flat indices stay below 2^31 rows per (b, h) and 2^24 positions (exact in fp32)
     if (N > (1 << 24) || static_cast<long long>(B) * H > (1LL << 31) - 1) return ALIBI_ERR_UNSUPPORTED;
+    // prefill work items and 256-key blocks of every (b, h) are counted in int
+    if (static_cast<long long>(B) * H * ((N + 255) / 256) > (1LL << 31) - 1) return ALIBI_ERR_UNSUPPORTED;
     return ALIBI_OK;
 }
 
@@ -433,6 +458,36 @@ int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int H, int N,
     Slopes s;
     fill_slopes(H, &s);
     return to_status(launch_underflow(q, k, B, H, N, d, tau, counts, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_decode_underflow_bf16(const void *q, const void *kcache, int B, int H, int L, int d, float tau,
+                                unsigned long long *counts, void *stream)
+{
+    if (!q || !kcache || !counts) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(kcache) || (reinterpret_cast<uintptr_t>(counts) & 7u)) return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, L, d);
+    if (st != ALIBI_OK) return st;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (!std::isfinite(tau)) return ALIBI_ERR_INVALID;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_decode_underflow(q, kcache, B, H, L, d, tau, counts, s, static_cast<cudaStream_t>(stream)));
+}
+
+int alibi_selftest_fwd_timeout(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                               int N, int d, int wait_us, void *stream)
+{
+    if (!q || !k || !v || !out) return ALIBI_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lse && !aligned16(lse)))
+        return ALIBI_ERR_INVALID;
+    int st = check_dims(B, H, N, d);
+    if (st != ALIBI_OK) return st;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
+    if (wait_us < 1 || wait_us > 1000000) return ALIBI_ERR_INVALID;
+    Slopes s;
+    fill_slopes(H, &s);
+    return to_status(launch_fwd_tc(q, k, v, out, lse, B, H, N, d, 1, 0u, 0.0f, 0.0f, s,
+                                   static_cast<cudaStream_t>(stream), static_cast<uint64_t>(wait_us) * 1000u));
 }
 
 int alibi_selftest_timeout(void *stream)

@@ -191,12 +191,85 @@ __global__ void __launch_bounds__(kUfRows) underflow_kernel(const __nv_bfloat16 
     }
 }
 
+// Decode row (query at position L-1 against keys 0..L-1): one CTA per (b, h), 256
+// threads, LPK = D/8 lanes per key row (16-byte loads). Pass 1 takes the row max of
+// x_j = q.k_j / sqrt(d) - m_h (L-1-j), pass 2 counts the keys with x_j - M <= tau.
+template <int D>
+__global__ void __launch_bounds__(256) decode_underflow_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                               const __nv_bfloat16 *__restrict__ k,
+                                                               unsigned long long *__restrict__ counts, int H, int L,
+                                                               float tau, float scale, Slopes slopes)
+{
+    constexpr int LPK = D / 8, KPW = 32 / LPK;  // lanes per key, keys per warp pass
+    __shared__ float redf[8];
+    __shared__ unsigned long long redc[8];
+    const int bh = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LPK, l = lane % LPK;
+    const float slope = slopes.nat[bh % H];
+    const __nv_bfloat16 *kb = k + static_cast<size_t>(bh) * L * D;
+    float qf[8];
+    {
+        const uint4 u = *reinterpret_cast<const uint4 *>(q + static_cast<size_t>(bh) * D + 8 * l);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            qf[2 * t] = __uint_as_float(w[t] << 16);
+            qf[2 * t + 1] = __uint_as_float(w[t] & 0xFFFF0000u);
+        }
+    }
+    float M = -INFINITY;
+    unsigned long long cnt = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int j0 = warp * KPW; j0 < L; j0 += 8 * KPW) {
+            const int j = j0 + sub;
+            float dot = 0.f;
+            if (j < L) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(j) * D + 8 * l);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    dot = fmaf(qf[2 * t], __uint_as_float(w[t] << 16), dot);
+                    dot = fmaf(qf[2 * t + 1], __uint_as_float(w[t] & 0xFFFF0000u), dot);
+                }
+            }
+#pragma unroll
+            for (int o = LPK / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            if (j < L && l == 0) {
+                const float x = fmaf(dot, scale, -slope * static_cast<float>(L - 1 - j));
+                if (pass == 0)
+                    M = fmaxf(M, x);
+                else
+                    cnt += (x - M <= tau) ? 1ull : 0ull;
+            }
+        }
+        if (pass == 0) {  // CTA-wide row max
+#pragma unroll
+            for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            if (lane == 0) redf[warp] = M;
+            __syncthreads();
+            M = redf[0];
+            for (int w = 1; w < 8; ++w) M = fmaxf(M, redf[w]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) redc[warp] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long s = 0;
+        for (int w = 0; w < 8; ++w) s += redc[w];
+        atomicAdd(&counts[bh % H], s);
+    }
+}
+
 // Waits on a barrier nobody arrives on: the bounded wait must give up and record
 // a timeout (failure-path self-test).
 __global__ void selftest_timeout_kernel(uint32_t *err)
 {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
+        cta_err_init(kWaitLimitNs);
         mbar_init(&bar, 1);
         fence_mbar_init();
         mbar_wait(&bar, 0, err, 0x901);
@@ -251,6 +324,30 @@ cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, f
     probs_f32_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(q, k, lse, P, total, H, N, d, causal,
                                                                             1.0f / sqrtf(static_cast<float>(d)),
                                                                             slopes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_underflow(const void *q, const void *kc, int B, int H, int L, int d, float tau,
+                                    unsigned long long *counts, const Slopes &slopes, cudaStream_t stream)
+{
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(unsigned long long) * H, stream);
+    if (e != cudaSuccess) return e;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(BH);
+    const float scale = 1.0f / sqrtf(static_cast<float>(d));
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(kc);
+    if (d == 128)
+        decode_underflow_kernel<128><<<grid, 256, 0, stream>>>(qb, kb, counts, H, L, tau, scale, slopes);
+    else if (d == 64)
+        decode_underflow_kernel<64><<<grid, 256, 0, stream>>>(qb, kb, counts, H, L, tau, scale, slopes);
+    else if (d == 32)
+        decode_underflow_kernel<32><<<grid, 256, 0, stream>>>(qb, kb, counts, H, L, tau, scale, slopes);
+    else if (d == 16)
+        decode_underflow_kernel<16><<<grid, 256, 0, stream>>>(qb, kb, counts, H, L, tau, scale, slopes);
+    else
+        return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

@@ -47,18 +47,21 @@ __device__ __forceinline__ void bf16x8(const uint4 &u, float (&f)[8])
     }
 }
 
-// Max squared key norm per (b, h): grid (key blocks, B*H), 256 threads, LPK lanes per key.
+// Max squared key norm per (b, h): a one-dimensional grid of nblk 256-key blocks per
+// (b, h) (so B*H may exceed the 65535 limit of a second grid dimension), 256
+// threads, LPK lanes per key.
 template <int D>
-__global__ void __launch_bounds__(256) kmax_kernel(const __nv_bfloat16 *__restrict__ k, int N,
+__global__ void __launch_bounds__(256) kmax_kernel(const __nv_bfloat16 *__restrict__ k, int N, int nblk,
                                                    unsigned int *__restrict__ kmax2_bits)
 {
     constexpr int LPK = D / 8, KPW = 32 / LPK;  // lanes per key, keys per warp pass
-    const int bh = blockIdx.y;
+    const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(nblk));
+    const int blk = static_cast<int>(blockIdx.x - static_cast<unsigned>(bh) * nblk);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane / LPK, l = lane % LPK;
     const __nv_bfloat16 *kb = k + static_cast<size_t>(bh) * N * D;
     float best = 0.f;
-    for (int j0 = blockIdx.x * 256 + warp * KPW; j0 < min(N, (blockIdx.x + 1) * 256); j0 += 8 * KPW) {
+    for (int j0 = blk * 256 + warp * KPW; j0 < min(N, (blk + 1) * 256); j0 += 8 * KPW) {
         const int j = j0 + sub;
         float s = 0.f;
         if (j < N) {
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(const int2 *__restrict_
     __syncthreads();
     for (int w = threadIdx.x; w < items; w += blockDim.x) atomicAdd(&hist[info[w].y], 1);
     __syncthreads();
-    if (threadIdx.x == 0) {  // exclusive offsets, longest first (max_len <= 16384 bins)
+    if (threadIdx.x == 0) {  // exclusive offsets, longest first (at most 12288 bins)
         int acc = 0;
         for (int b = max_len; b >= 0; --b) {
             const int c = hist[b];
@@ -197,25 +200,28 @@ cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, 
     const float c1 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
-    dim3 g1((N + 255) / 256, BH);
+    const int nblk = (N + 255) / 256;
+    const unsigned g1 = static_cast<unsigned>(nblk) * static_cast<unsigned>(BH);  // <= 2^31 - 1 (check_dims)
     if (d == 128) {
-        kmax_kernel<128><<<g1, 256, 0, stream>>>(kb, N, kmax2);
+        kmax_kernel<128><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
         item_plan_kernel<128><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
     } else if (d == 64) {
-        kmax_kernel<64><<<g1, 256, 0, stream>>>(kb, N, kmax2);
+        kmax_kernel<64><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
         item_plan_kernel<64><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
     } else if (d == 32) {
-        kmax_kernel<32><<<g1, 256, 0, stream>>>(kb, N, kmax2);
+        kmax_kernel<32><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
         item_plan_kernel<32><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
     } else if (d == 16) {
-        kmax_kernel<16><<<g1, 256, 0, stream>>>(kb, N, kmax2);
+        kmax_kernel<16><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
         item_plan_kernel<16><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
     } else {
         return cudaErrorInvalidValue;
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int max_len = NQT;  // no item spans more tiles than there are tiles
-    if (max_len + 1 <= 16384) {
+    // one int per bin within the 48 KB of dynamic shared memory a launch gets without
+    // raising the kernel's attribute; beyond that the nominal order is kept
+    if ((max_len + 1) * sizeof(int) <= 48 * 1024) {
         plan_sort_kernel<<<1, 1024, (max_len + 1) * sizeof(int), stream>>>(info, items, max_len, plan);
     } else {
         plan_identity_kernel<<<(items + 255) / 256, 256, 0, stream>>>(info, items, plan);

@@ -28,6 +28,11 @@ uint32_t *device_status_word();  // per current device, 2 words
 void fill_slopes(int H, Slopes *s);
 void fill_slopes_from(int H, const float *nat, Slopes *s);  // caller-chosen slopes (natural-log units)
 int num_sms();                   // of the current device
+// Once per (current device, kernel): check that `func` compiled to `regs` registers
+// per thread (0: any count) and raise its dynamic shared-memory limit to `smem`
+// bytes. Function attributes belong to each device's context, so a process that
+// runs on several devices prepares each one.
+cudaError_t prepare_kernel(const void *func, int smem, uint32_t regs);
 cudaMemPool_t decode_pool();     // library-owned stream-ordered pool of the current device
 // 3-D TMA map over a [dim2, dim1, dim0] bf16 tensor (dim0 fastest), box {box0, box1, 1},
 // zero fill out of bounds; 128-byte swizzle, or none (plain row-major boxes, as the
@@ -67,7 +72,7 @@ cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, 
 // Kernel launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
                           int N, int d, int causal, unsigned int flags, float clamp_min, float softcap_z, const Slopes &slopes,
-                          cudaStream_t stream);
+                          cudaStream_t stream, uint64_t test_wait_ns = 0);
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B,
                            int H, int N, int d, int causal, const Slopes &slopes, cudaStream_t stream);
 cudaError_t launch_probs_f32(const float *q, const float *k, const float *lse, float *P, int B, int H, int N,
@@ -84,5 +89,7 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
 cudaError_t launch_selftest_timeout(cudaStream_t stream);
 cudaError_t launch_underflow(const void *q, const void *k, int B, int H, int N, int d, float tau,
                              unsigned long long *counts, const Slopes &slopes, cudaStream_t stream);
+cudaError_t launch_decode_underflow(const void *q, const void *kc, int B, int H, int L, int d, float tau,
+                                    unsigned long long *counts, const Slopes &slopes, cudaStream_t stream);
 
 }  // namespace alibi

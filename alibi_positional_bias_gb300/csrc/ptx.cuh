@@ -67,11 +67,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed, for at most
-// about kWaitLimitNs. Returns false (and records ALIBI_DEV_TIMEOUT) on expiry,
-// or early if another thread already recorded an error. The error word (a
-// global load) and the global timer are read only every 256 polls, so a
-// completed phase is noticed without an L2 round trip on the critical path.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -85,7 +80,33 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t site)
+// This CTA's failure state, in static shared memory: the abort code one of the
+// CTA's own roles raised, and the limit of every bounded wait. Their addresses are
+// constants, so a wait carries no extra register. Waits give up early only on the
+// CTA's own abort code, never on the device status word, so an error left
+// uncollected in that word by an earlier launch does not cut a later launch short,
+// while one role's timeout still stops the other roles of its CTA within a few
+// hundred polls. A kernel that waits calls cta_err_init() from one thread before
+// its first barrier.
+static __shared__ uint32_t cta_abort;
+static __shared__ uint64_t cta_wait_ns;
+
+__device__ __forceinline__ void cta_err_init(uint64_t limit_ns)
+{
+    cta_abort = 0u;
+    cta_wait_ns = limit_ns;
+}
+
+// Wait until the phase with the given parity has completed, for at most the CTA's
+// wait limit. Returns false on expiry, after recording ALIBI_DEV_TIMEOUT in the
+// device status word `err` and in the CTA's abort code; or early if another role
+// of this CTA raised an error (unless `drain`: a drain wait is for work this thread
+// issued itself, which completes on its own, so it ignores the abort code and ends
+// only on completion or its own time limit). The abort code and the global timer
+// are read only every 256 polls, so a completed phase is noticed without extra
+// latency on the critical path.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t site,
+                                          bool drain = false)
 {
     if (mbar_test(bar, parity)) return true;  // already complete: no suspend
     uint64_t t0 = 0;
@@ -93,12 +114,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     for (uint32_t n = 0;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 255u) == 255u) {
-            if (*(volatile uint32_t *)err != 0u) return false;
+            if (!drain && *(volatile uint32_t *)&cta_abort != 0u) return false;
             const uint64_t t = global_timer_ns();
             if (t0 == 0) {
                 t0 = t;
-            } else if (t - t0 > kWaitLimitNs) {
+            } else if (t - t0 > *(volatile uint64_t *)&cta_wait_ns) {
                 report_error(err, ALIBI_DEV_TIMEOUT, site);
+                *(volatile uint32_t *)&cta_abort = ALIBI_DEV_TIMEOUT;
                 return false;
             }
         }

@@ -292,6 +292,19 @@ ALIBI_API int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int
                               unsigned long long *counts, void *stream);
 
 /*
+ * The same count for the decode row ("When Attention Goes Blind", sec. 3.2-3.3,
+ * applied to the query at position L-1 of "ALiBi: Attention with Linear Biases",
+ * the KV-cache paragraph): per head h, summed over b, the number of cached keys j
+ * (0 <= j < L) whose max-subtracted exponent x_j - M is <= tau, with
+ * x_j = q.k_j/sqrt(d) - m_h (L-1-j) and M = max_j x_j. Two passes over K in
+ * fp32. q: device bf16 [B, H, d]; kcache: device bf16 [B, H, L, d]; counts:
+ * device uint64 [H], overwritten (zeroed on `stream` first). d in
+ * {16, 32, 64, 128}. Reporting only (it reads K twice).
+ */
+ALIBI_API int alibi_decode_underflow_bf16(const void *q, const void *kcache, int B, int H, int L, int d, float tau,
+                                          unsigned long long *counts, void *stream);
+
+/*
  * Self-test of the failure path; the pages have no counterpart to it. Launches
  * one CTA whose thread waits on a shared-memory barrier that nothing ever
  * arrives on, through the same bounded wait every kernel uses. After about one
@@ -303,10 +316,29 @@ ALIBI_API int alibi_attn_underflow_bf16(const void *q, const void *k, int B, int
 ALIBI_API int alibi_selftest_timeout(void *stream);
 
 /*
+ * Self-test of the failure path through the bf16 prefill kernel itself; the
+ * pages have no counterpart to it. Runs alibi_attn_fwd on the caller's buffers
+ * (same arguments, layouts and checks) with two changes: each CTA's TMA producer
+ * leaves out the load of its first work item's first Q tile, and every bounded
+ * wait gives up after wait_us microseconds (1 <= wait_us <= 1000000). The MMA
+ * issuer's wait for that tile runs out; the kernel records ALIBI_ERR_TIMEOUT in
+ * the device status word, its other roles stop at their next wait, every load
+ * and MMA already issued is waited for, TMEM is freed and the kernel returns.
+ * out and lse are left undefined. alibi_check_error(stream) then returns
+ * ALIBI_ERR_TIMEOUT and the context stays usable. No fault, trap or hang is
+ * involved.
+ */
+ALIBI_API int alibi_selftest_fwd_timeout(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                                         int H, int N, int d, int wait_us, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the device status word of the
  * current device. Returns ALIBI_ERR_TIMEOUT if a kernel gave up a bounded
  * wait since the last check, ALIBI_ERR_CUDA if the stream reports an error,
- * else ALIBI_OK.
+ * else ALIBI_OK. The word accumulates until it is collected here, but an
+ * uncollected error does not affect later calls: a kernel's waits give up early
+ * only on a failure inside the same CTA, so calls made after a timeout compute
+ * their results normally (the timeout is still reported by the next check).
  */
 ALIBI_API int alibi_check_error(void *stream);
 

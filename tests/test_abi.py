@@ -143,6 +143,19 @@ def test_decode_and_aux_argument_errors(lib):
         ab.ALIBI_ERR_UNSUPPORTED
     assert lib.alibi_attn_underflow_bf16(P, P, 1, 1, 8, 64, ctypes.c_float(float("nan")), P, None) == \
         ab.ALIBI_ERR_INVALID
+    st = lib.alibi_selftest_fwd_timeout
+    assert st(P, P, P, P, P, 1, 1, 8, 64, 0, None) == ab.ALIBI_ERR_INVALID          # wait limit below 1 us
+    assert st(P, P, P, P, P, 1, 1, 8, 64, 1000001, None) == ab.ALIBI_ERR_INVALID    # above one second
+    assert st(None, P, P, P, P, 1, 1, 8, 64, 100, None) == ab.ALIBI_ERR_INVALID
+    assert st(P, P, P, P, P, 1, 1, 8, 48, 100, None) == ab.ALIBI_ERR_UNSUPPORTED
+
+
+def test_large_head_counts_are_bounded_on_the_host(lib):
+    # work items (256-row blocks of every (b, h)) are counted in 32-bit integers:
+    # B*H*ceil(N/256) beyond 2^31 - 1 is refused before any launch
+    f = lib.alibi_attn_fwd
+    assert f(P, P, P, P, P, 1 << 16, 1 << 8, 1 << 15, 64, 1, None) == ab.ALIBI_ERR_UNSUPPORTED
+    assert lib.alibi_attn_skip_plan(P, P, 1 << 16, 1 << 8, 1 << 15, 64, None, P, None) == ab.ALIBI_ERR_UNSUPPORTED
 
 
 def test_explicit_slopes_bit_exact_vs_oracle(lib):

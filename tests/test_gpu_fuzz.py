@@ -33,7 +33,7 @@ COMBOS = [c for r in (1, 2, 3) for c in itertools.combinations(("clamp", "logdis
 
 
 def _length(rng, top):
-    if rng.random() < 0.4 and top >= 127:  # one key either side of a tile edge, or on it
+    if rng.random() < 0.4 and top >= 128:  # one key either side of a tile edge, or on it
         return int(min(top, max(1, 128 * int(rng.integers(1, top // 128 + 1)) + int(rng.integers(-1, 2)))))
     return int(min(top, max(1, round(np.exp(rng.uniform(0.0, np.log(top)))))))
 

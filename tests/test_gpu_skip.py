@@ -107,3 +107,37 @@ def test_skipped_entries_truly_underflow():
         assert (skipped * math.log2(math.e) <= -126.0).all()
         checked += 1
     assert checked > 5
+
+
+def test_skip_more_heads_than_grid_rows(ab):
+    # B*H = 70000 (b, h) pairs, past the 65535 a second grid dimension holds: the
+    # plan's key-norm pass runs on a one-dimensional grid. N = 300 gives every head
+    # a second 256-row block whose far tiles the steep heads of the 100-head
+    # schedule leave out; the output must stay bit-identical to the dense kernel.
+    import torch
+    B, H, N, d = 700, 100, 300, 16
+    g = torch.Generator(device="cuda").manual_seed(70000)
+    q, k, v = (torch.randn((B, H, N, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    o0, l0 = ab.alibi_attn_fwd(q, k, v)
+    o1, l1 = ab.alibi_attn_fwd(q, k, v, skip_underflow=True)
+    plan = ab.alibi_attn_skip_plan(q, k).cpu().numpy()
+    ab.alibi_check_error()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert plan.max() > 0  # some tiles were left out
+
+
+@pytest.mark.parametrize("N", [1_540_000, 1_600_000])
+def test_skip_plan_longest_sequences(ab, N):
+    # The plan's work order is a counting sort over item lengths in one CTA's
+    # shared memory (one int per possible length: 128-key tiles + 1). At 1.54M keys
+    # the 12033 bins still fit the 48 KB a launch gets by default; at 1.6M (12501
+    # bins) the plan keeps the nominal order instead. Both stay bit-identical to
+    # the dense kernel.
+    import torch
+    B, H, d = 1, 1, 16
+    g = torch.Generator(device="cuda").manual_seed(N)
+    q, k, v = (torch.randn((B, H, N, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    o0, l0 = ab.alibi_attn_fwd(q, k, v)
+    o1, l1 = ab.alibi_attn_fwd(q, k, v, skip_underflow=True)
+    ab.alibi_check_error()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
