@@ -128,6 +128,26 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU (oracle)
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def oracle_prefill_sample(w, budget_s: float, seed: int = 0):
     """Time the fp64 oracle on sampled rows of the prefill workload. Returns
     (causal FLOPs of the rows, seconds, rows, threads)."""
@@ -208,7 +228,8 @@ def run_reference(args):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{PREFILL} (B=1, H=16, N=16384, d=128, causal) prefill rows, fp64 oracle",
                    "global_batch": wp.B, "seq_len": wp.N, "parallelism": "host threads"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(),
+                         "kind": "oracle",
                          "sample": f"{rows} query rows of one head of {PREFILL}, spread over positions; "
                                    f"~{per_step:.0f} s of CPU work per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -393,6 +414,7 @@ def run_native(args):
     # -------------------- exact underflow-tile skipping, same inputs, own timing
     skip = noncausal = steep = backward = None
     others = None
+    uf_configs = {}  # underflow fraction of every bf16 configuration (reported, untimed)
     if do_pre:
         tiles_run, tiles_all = tiles_kept(ab.alibi_attn_skip_plan(q, k).cpu().numpy())
         t_skip = timed_ms(lambda: ab.alibi_attn_fwd(q, k, v, out=out, lse=lse, stream=stream, skip_underflow=True))
@@ -450,6 +472,8 @@ def run_native(args):
             tf = prefill_flops(wo) / (t_o / 1e3) / 1e12
             others[name] = {"shape": f"B={wo.B} H={wo.H} N={wo.N} d={wo.d}", "ms": t_o, "tflops": world * tf,
                             "frac": tf / peaks["bf16_tflops"]}
+            if not args.no_underflow:
+                uf_configs[name] = underflow_report(ab, wo, to[0], to[1], stream)
             if name == "layer_n2048":
                 # the decoder-layer training shape's backward (dO ~ N(0, 1) from its own seed)
                 dob = torch.empty_like(to[0])
@@ -626,17 +650,18 @@ def run_native(args):
     # ------------------------------------------ underflow fraction (reported, untimed)
     underflow = None
     if not args.no_underflow:
-        tau = math.log(2.0 ** -126)
-        counts = ab.alibi_attn_underflow_bf16(q, k, tau).cpu().numpy().astype(np.float64)
-        pairs_per_head = wp.B * wp.N * (wp.N + 1) / 2
-        underflow = {"tau": "ln 2^-126", "fraction": float(counts.sum() / (pairs_per_head * wp.H)),
-                     "per_head": [round(float(c / pairs_per_head), 4) for c in counts]}
+        uf_configs[PREFILL] = underflow_report(ab, wp, q, k, stream)
+        uf_configs[DECODE] = underflow_report(ab, wd, dq, dk, stream)
+        underflow = {"tau": "ln 2^-126 (the threshold the paper's printed numbers follow)",
+                     "fraction": uf_configs[PREFILL]["fraction"], "per_head": uf_configs[PREFILL]["per_head"],
+                     "per_config": {n: uf_configs[n] for n in ("heads6_n1024", "layer_n2048", PREFILL, DECODE)
+                                    if n in uf_configs}}
 
     # ------------------------------------------------------ CPU baseline (oracle)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, s, rows, threads = oracle_prefill_sample(wp, args.cpu_seconds)
-        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(), "kind": "oracle",
                "sample": f"{rows} query rows of one head of {PREFILL} (causal FLOPs 4 (i+1) d per row), "
                          f"fp64, {s:.1f} s"}
 
@@ -701,6 +726,34 @@ def run_native(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def underflow_report(ab, w, q, k, stream) -> dict:
+    """Fraction of attention weights whose max-subtracted exponent is <= ln 2^-126
+    ("When Attention Goes Blind" sec. 3.2-3.3), counted by the library's kernels:
+    every causal pair of a prefill workload, or every cached key of each decode
+    query row. Beside it, the closed form the paper's Fig. 1 assumes (content
+    scores A = 0): a key at distance D underflows iff m_h D >= -tau."""
+    tau = math.log(2.0 ** -126)
+    slopes = [float(x) for x in ab.alibi_slopes(w.H)]
+    if w.kind == "decode":
+        counts = ab.alibi_decode_underflow_bf16(q, k, tau, stream=stream).cpu().tolist()
+        per_head_entries = w.B * w.N
+        a0 = [max(0, w.N - math.ceil(-tau / m)) / w.N for m in slopes]
+        what = "cached keys of the decode query rows (position L-1)"
+    else:
+        counts = ab.alibi_attn_underflow_bf16(q, k, tau, stream=stream).cpu().tolist()
+        per_head_entries = w.B * w.N * (w.N + 1) / 2
+        a0 = []
+        for m in slopes:
+            dist = math.ceil(-tau / m)
+            a0.append((w.N - dist) * (w.N - dist + 1) / 2 / (w.N * (w.N + 1) / 2) if dist < w.N else 0.0)
+        what = "causal pairs"
+    ab.alibi_check_error(stream)
+    return {"shape": f"B={w.B} H={w.H} N={w.N} d={w.d}", "counted": what,
+            "fraction": float(sum(counts) / (per_head_entries * w.H)),
+            "per_head": [round(float(c / per_head_entries), 4) for c in counts],
+            "a0_closed_form": float(sum(a0) / w.H)}
 
 
 def load_traffic() -> dict:

@@ -68,3 +68,24 @@ def test_counts_more_heads_than_grid_rows(ab):
     want, near = oracle.underflow_counts_per_head(q.f32, k.f32, TAU_D, band=band_for(w.H, w.N))
     diff = np.abs(got - want.astype(np.int64))
     assert (diff <= near.astype(np.int64)).all(), (got, want, near)
+
+
+@pytest.mark.parametrize("B,H,L,d", [(2, 40, 8192, 128), (3, 5, 1000, 64), (1, 4, 1, 128), (2, 3, 777, 16)])
+def test_decode_row_counts_match_oracle(ab, B, H, L, d):
+    # The decode row is prefill row L-1 of the same sequence ("ALiBi: Attention with
+    # Linear Biases", KV-cache paragraph): the oracle counts it as that row of a
+    # prefill problem whose other query rows are never read.
+    w = gen.Workload("ufdec", "decode", B, H, L, d, "bf16", seed=23 + L)
+    q, k, _ = gen.generate(w)
+    c = ab.alibi_decode_underflow_bf16(dev(q, "bf16"), dev(k, "bf16"), TAU_D)
+    ab.alibi_check_error()
+    got = c.cpu().numpy().astype(np.int64)
+    qfull = np.zeros((B, H, L, d), np.float32)
+    qfull[:, :, L - 1] = q.f32
+    rows = np.arange(B * H, dtype=np.int64) * L + (L - 1)
+    cnt, near = oracle.underflow_rows(qfull, k.f32, TAU_D, rows=rows, band=band_for(H, L))
+    want = cnt.reshape(B, H).sum(0).astype(np.int64)
+    nr = near.reshape(B, H).sum(0).astype(np.int64)
+    assert (np.abs(got - want) <= nr).all(), (got, want, nr)
+    if L > 2000:
+        assert want.sum() > 0  # the steep heads do underflow at this length
