@@ -78,6 +78,31 @@ struct Cfg {
     static constexpr uint32_t kSmem = kBar + 256 + 1024;   // barriers, TMEM slot, alignment slack
 };
 
+// Division by a runtime divisor d >= 1 of numerators below 2^31 as a multiply-high,
+// an add and a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d)
+// + 1, n / d = (umulhi(n, m) + n) >> l. The work-item decoding runs it at every item
+// boundary, where a plain integer division is a long dependent sequence.
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+static FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv &f)
+{
+    const uint32_t u = static_cast<uint32_t>(n);
+    return static_cast<int>((__umulhi(u, f.m) + u) >> f.l);
+}
+
+__device__ __forceinline__ int fmod_(int n, const FastDiv &f) { return n - fdiv(n, f) * static_cast<int>(f.d); }
+
 struct FwdParams {
     CUtensorMap tq, tk, tv;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
     CUtensorMap tout;        // [BH, N, d] bf16, box {32, 32, 1}, no swizzle (epilogue stores)
@@ -87,6 +112,7 @@ struct FwdParams {
     uint64_t wait_ns;  // limit of every bounded wait
     int test_skip_q0;  // failure-path self-test: the producer leaves out the first item's Q tile 0
     int N, BH, H, NQB, NQT, num_items;
+    FastDiv div_bh, div_h, div_nqb;  // by B*H, H and NQB
     int dr;  // the tensors' head size (<= D: the D = 64 kernel also serves d = 16 and 32)
     int causal;  // 1: keys j <= i only; 0: every key, distance |i - j|
     float c1;  // log2(e) / sqrt(d)
@@ -172,11 +198,11 @@ __device__ __forceinline__ Item decode_item(const FwdParams &p, int idx, bool ca
     int first = 0;
     if (p.plan) {
         const int2 e = p.plan[idx];
-        it.bh = e.x / p.NQB;
+        it.bh = fdiv(e.x, p.div_nqb);
         it.qb = e.x - it.bh * p.NQB;
         first = e.y;
     } else {
-        const int round = idx / p.BH;
+        const int round = fdiv(idx, p.div_bh);
         it.bh = idx - round * p.BH;
         it.qb = p.NQB - 1 - round;
     }
@@ -407,13 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     }
                     for (int s = 0; s < 2 && ok; ++s) {
                         if (slot_active(t, s, it, CAUSAL)) {
-                            ok = mbar_wait(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
+                            ok = mbar_wait_spin(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
                             if (ok && first_pv[s]) ok = mbar_wait(&o_empty[s], (o_cnt[s] & 1) ^ 1, err, SITE_MMA_O);
                             ok = __all_sync(0xffffffffu, ok);
                             if (!ok) break;
                             tc_fence_after();
                             issue_PV_half(s, vst, first_pv[s], 0);
-                            ok = mbar_wait(&p_hi[s], p_cnt[s] & 1, err, SITE_MMA_P);
+                            ok = mbar_wait_spin(&p_hi[s], p_cnt[s] & 1, err, SITE_MMA_P);
                             ++p_cnt[s];
                             ok = __all_sync(0xffffffffu, ok);
                             if (!ok) break;
@@ -463,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     const int wn = item_index(kk);
                     if (wn >= p.num_items) return;
                     const Item tn = decode_item(p, wn, CAUSAL);
-                    const float bv = p.slopes.log2e[tn.bh % p.H] * static_cast<float>(r) / p.c1;
+                    const float bv = p.slopes.log2e[fmod_(tn.bh, p.div_h)] * static_cast<float>(r) / p.c1;
                     write_bias_row(smem + C::kAux, r, kk & 1, bv);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -475,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             if (s == 1 && !t.q1valid) continue;
             const int qt = 2 * t.qb + s;
             const int i = qt * BM + r;
-            const float sl2 = p.slopes.log2e[t.bh % p.H];
+            const float sl2 = p.slopes.log2e[fmod_(t.bh, p.div_h)];
             const int it0 = (s == 0 && t.q1valid && CAUSAL) ? 1 : 0;
             float M = -INFINITY, l = 0.f;
             for (int it = it0; it < t.n; ++it) {
@@ -510,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                     //            -m log2(D + 1) in base 2), clamped from below.
                     const bool cap = p.variant & kFwdSoftcap, logd = p.variant & kFwdLogDist,
                                clamp = p.variant & kFwdClamp;
-                    const float mnat = p.slopes.nat[t.bh % p.H];
+                    const float mnat = p.slopes.nat[fmod_(t.bh, p.div_h)];
                     const float di = static_cast<float>(i - j * BN);  // exact: |i - k0| < 2^24
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
@@ -711,6 +737,9 @@ static cudaError_t launch_fwd_tc_d(const void *q, const void *k, const void *v, 
     p.NQT = (N + BM - 1) / BM;
     p.NQB = (p.NQT + 1) / 2;
     p.num_items = p.NQB * p.BH;
+    p.div_bh = make_fastdiv(static_cast<uint32_t>(p.BH));
+    p.div_h = make_fastdiv(static_cast<uint32_t>(H));
+    p.div_nqb = make_fastdiv(static_cast<uint32_t>(p.NQB));
     p.causal = causal;
     p.c1 = 1.4426950408889634f / sqrtf(static_cast<float>(dr));
     p.slopes = slopes;

@@ -127,6 +127,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     }
 }
 
+// The same bounded wait polling with the non-suspending test: for a single issuing
+// warp whose reaction time to a handoff is on the critical path (the suspending
+// try_wait wakes a little later after the phase completes).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, uint32_t *err, uint32_t site)
+{
+    uint64_t t0 = 0;
+#pragma unroll 1
+    for (uint32_t n = 0;; ++n) {
+        if (mbar_test(bar, parity)) return true;
+        if ((n & 1023u) == 1023u) {
+            if (*(volatile uint32_t *)&cta_abort != 0u) return false;
+            const uint64_t t = global_timer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > *(volatile uint64_t *)&cta_wait_ns) {
+                report_error(err, ALIBI_DEV_TIMEOUT, site);
+                *(volatile uint32_t *)&cta_abort = ALIBI_DEV_TIMEOUT;
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
