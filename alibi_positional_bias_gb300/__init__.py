@@ -28,7 +28,7 @@ __all__ = [
     "alibi_kv_block_norms", "alibi_attn_decode_skip",
 ]
 
-ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT = 0, -1, -2, -3, -4
+ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT, ALIBI_ERR_CHECK = 0, -1, -2, -3, -4, -5
 ALIBI_FWD_SKIP_UNDERFLOW, ALIBI_FWD_CLAMP, ALIBI_FWD_LOGDIST, ALIBI_FWD_SOFTCAP = 1, 2, 4, 8
 
 _lock = threading.Lock()
@@ -47,8 +47,14 @@ class AlibiError(RuntimeError):
         super().__init__(f"{where}: {alibi_status_str(status)} ({status})")
 
 
+def checks_build() -> bool:
+    """True when ALIBI_CHECKS=1 selects the debug-checks library (every TMA coordinate,
+    TMEM address and shared-memory operand tested in the kernels; slower)."""
+    return os.environ.get("ALIBI_CHECKS", "0") == "1"
+
+
 def lib_path() -> str:
-    return _build.LIB
+    return _build.LIB_CHECKS if checks_build() else _build.LIB
 
 
 def load(build_if_missing: bool = False):
@@ -57,9 +63,9 @@ def load(build_if_missing: bool = False):
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB
+        path = lib_path()
         if build_if_missing and not os.path.exists(path):
-            _build.build()
+            _build.build(checks=checks_build())
         if not os.path.exists(path):
             raise RuntimeError(f"ALiBi CUDA library not built ({path}); run __graft_entry__.build()")
         lib = ctypes.CDLL(path)

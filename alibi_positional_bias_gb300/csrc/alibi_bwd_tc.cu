@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         cta_err_init(kWaitLimitNs);
+        cta_check_init(p.err, smem_raw, C::kSmem);
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
         for (int s = 0; s < 2; ++s) {
@@ -637,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 
     if (threadIdx.x == 0) {
         cta_err_init(kWaitLimitNs);
+        cta_check_init(p.err, smem_raw, C::kSmem);
         mbar_init(qd_full, 1);
         mbar_init(qd_empty, 1);
         for (int s = 0; s < 2; ++s) {

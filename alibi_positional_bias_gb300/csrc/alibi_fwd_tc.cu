@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
 
     if (threadIdx.x == 0) {
         cta_err_init(p.wait_ns);
+        cta_check_init(p.err, smem_raw, C::kSmem);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&q_full[s], 1);
             mbar_init(&k_full[s], 1);

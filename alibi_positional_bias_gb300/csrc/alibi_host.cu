@@ -201,6 +201,7 @@ const char *alibi_status_str(int status)
         case ALIBI_ERR_UNSUPPORTED: return "ALIBI_ERR_UNSUPPORTED: unsupported shape or option";
         case ALIBI_ERR_CUDA: return "ALIBI_ERR_CUDA: CUDA call or kernel launch failed";
         case ALIBI_ERR_TIMEOUT: return "ALIBI_ERR_TIMEOUT: a bounded device-side wait expired";
+        case ALIBI_ERR_CHECK: return "ALIBI_ERR_CHECK: a debug-build address check failed";
         default: return "unknown alibi status";
     }
 }
@@ -503,6 +504,7 @@ int alibi_check_error(void *stream)
     uint32_t h[2] = {0, 0};
     if (cudaMemcpy(h, w, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ALIBI_ERR_CUDA;
     if (h[0] != 0u && cudaMemset(w, 0, sizeof(h)) != cudaSuccess) return ALIBI_ERR_CUDA;
+    if (h[0] & ALIBI_DEV_CHECK) return ALIBI_ERR_CHECK;
     if (h[0] & ALIBI_DEV_TIMEOUT) return ALIBI_ERR_TIMEOUT;
     if (h[0] != 0u) return ALIBI_ERR_CUDA;
     return ALIBI_OK;

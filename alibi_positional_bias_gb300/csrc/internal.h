@@ -11,6 +11,7 @@ namespace alibi {
 // Device status word bits (word 0) and the first failing site (word 1).
 constexpr uint32_t ALIBI_DEV_TIMEOUT = 1u;
 constexpr uint32_t ALIBI_DEV_BADSTATE = 2u;
+constexpr uint32_t ALIBI_DEV_CHECK = 4u;  // a debug-checks build found a bad address (checks.h)
 
 // Every device-side wait gives up after this long (ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "checks.h"
 #include "internal.h"
 
 namespace alibi {
@@ -97,6 +98,40 @@ __device__ __forceinline__ void cta_err_init(uint64_t limit_ns)
     cta_wait_ns = limit_ns;
 }
 
+// Debug-checks build (-DALIBI_CHECKS): the device status word and the CTA's dynamic
+// shared-memory window, against which the wrappers below test their addresses
+// (predicates in checks.h). Every CTA allocates all TMEM columns of its SM.
+#ifdef ALIBI_CHECKS
+static __shared__ uint32_t *cta_check_word;
+static __shared__ uint32_t cta_smem_lo, cta_smem_hi;
+constexpr uint32_t kCheckTmemCols = 512;
+
+__device__ __forceinline__ void check_fail(uint32_t id, uint32_t value)
+{
+    report_error(cta_check_word, ALIBI_DEV_CHECK, check::site(id, value));
+}
+
+__device__ __forceinline__ bool check_smem(uint32_t saddr, uint32_t bytes, uint32_t align)
+{
+    return check::smem_range(saddr, bytes, align, cta_smem_lo, cta_smem_hi);
+}
+#endif
+
+// One thread of every kernel that uses the wrappers below calls this before the
+// CTA's first barrier (a no-op outside the debug-checks build).
+__device__ __forceinline__ void cta_check_init(uint32_t *dev, const void *smem, uint32_t bytes)
+{
+#ifdef ALIBI_CHECKS
+    cta_check_word = dev;
+    cta_smem_lo = smem_u32(smem);
+    cta_smem_hi = cta_smem_lo + bytes;
+#else
+    (void)dev;
+    (void)smem;
+    (void)bytes;
+#endif
+}
+
 // Wait until the phase with the given parity has completed, for at most the CTA's
 // wait limit. Returns false on expiry, after recording ALIBI_DEV_TIMEOUT in the
 // device status word `err` and in the CTA's abort code; or early if another role
@@ -157,9 +192,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 3-D tiled load of one box into shared memory, completing on `bar`.
+// 3-D tiled load of one box into shared memory, completing on `bar`. Every load of
+// the kernels is a 16 KB box (64 bf16 x 128 rows) into a 1024-byte aligned swizzle atom.
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar)
 {
+#ifdef ALIBI_CHECKS
+    if (!check::tma_x_aligned(x)) return check_fail(check::TMA_LOAD, static_cast<uint32_t>(x));
+    if (!check_smem(smem_u32(dst), 16384, 1024)) return check_fail(check::TMA_LOAD, smem_u32(dst));
+#endif
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
@@ -172,6 +212,11 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
 // outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int x, int y, int z)
 {
+#ifdef ALIBI_CHECKS
+    if (!check::tma_store_coords(x, y, z))
+        return check_fail(check::TMA_STORE, static_cast<uint32_t>(x < 0 || (x & 7) ? x : (y < 0 ? y : z)));
+    if (!check_smem(smem_u32(src), 1024, 16)) return check_fail(check::TMA_STORE, smem_u32(src));
+#endif
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
                  "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
@@ -237,6 +282,29 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+#ifdef ALIBI_CHECKS
+// D columns (N of the instruction descriptor) inside the allocation and every shared-
+// memory operand's start inside the window; a TMEM A operand's K = 16 step (8 columns).
+__device__ __forceinline__ bool check_mma(uint32_t d_tmem, uint32_t idesc, const uint64_t *descs, int ndesc,
+                                          int a_tmem)
+{
+    if (!check::tmem_cols(d_tmem, check::idesc_n(idesc), kCheckTmemCols)) {
+        check_fail(check::TMEM_COLS, d_tmem);
+        return false;
+    }
+    if (a_tmem >= 0 && !check::tmem_cols(static_cast<uint32_t>(a_tmem), 8, kCheckTmemCols)) {
+        check_fail(check::TMEM_COLS, static_cast<uint32_t>(a_tmem));
+        return false;
+    }
+    for (int i = 0; i < ndesc; ++i)
+        if (!check_smem(check::desc_addr(descs[i]), 16, 16)) {
+            check_fail(check::SMEM_DESC, check::desc_addr(descs[i]));
+            return false;
+        }
+    return true;
+}
+#endif
+
 // Warp-converged forms: the whole warp executes the call with identical operands
 // and one elected lane (the lowest active one, i.e. the same lane every time
 // the warp is converged) issues the instruction. Keeping the issuing code
@@ -244,6 +312,10 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
+#ifdef ALIBI_CHECKS
+    const uint64_t descs[2] = {a_desc, b_desc};
+    if (!check_mma(d_tmem, idesc, descs, 2, -1)) return;
+#endif
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
@@ -259,6 +331,10 @@ __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint6
 // takes. Ordered with the issuing thread's MMAs; tracked by its commits.
 __device__ __forceinline__ void tmem_cp_w(uint32_t taddr, uint64_t s_desc)
 {
+#ifdef ALIBI_CHECKS
+    if (!check::tmem_cols(taddr, 8, kCheckTmemCols)) return check_fail(check::TMEM_COLS, taddr);
+    if (!check_smem(check::desc_addr(s_desc), 16, 16)) return check_fail(check::SMEM_DESC, check::desc_addr(s_desc));
+#endif
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
@@ -270,6 +346,9 @@ __device__ __forceinline__ void tmem_cp_w(uint32_t taddr, uint64_t s_desc)
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
+#ifdef ALIBI_CHECKS
+    if (!check_mma(d_tmem, idesc, &b_desc, 1, static_cast<int>(a_tmem & 0xFFFFu))) return;
+#endif
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
@@ -300,6 +379,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets row (lane base + t).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
+#ifdef ALIBI_CHECKS
+    // warp-uniform tests (the address is), so a skipped load is skipped by the whole warp
+    if (!check::tmem_cols(taddr, 32, kCheckTmemCols) || !check::tmem_lanes(taddr, threadIdx.x >> 5)) {
+        check_fail(check::tmem_cols(taddr, 32, kCheckTmemCols) ? check::TMEM_LANES : check::TMEM_COLS, taddr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+        return;
+    }
+#endif
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -314,6 +402,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
+#ifdef ALIBI_CHECKS
+    if (!check::tmem_cols(taddr, 32, kCheckTmemCols) || !check::tmem_lanes(taddr, threadIdx.x >> 5))
+        return check_fail(check::tmem_cols(taddr, 32, kCheckTmemCols) ? check::TMEM_LANES : check::TMEM_COLS, taddr);
+#endif
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"

@@ -48,7 +48,9 @@ typedef enum {
     ALIBI_ERR_INVALID = -1,     /* null pointer, non-positive size, misaligned pointer */
     ALIBI_ERR_UNSUPPORTED = -2, /* valid request the library does not implement (e.g. d) */
     ALIBI_ERR_CUDA = -3,        /* a CUDA runtime/driver call or kernel launch failed    */
-    ALIBI_ERR_TIMEOUT = -4      /* a bounded device-side wait expired (see alibi_check_error) */
+    ALIBI_ERR_TIMEOUT = -4,     /* a bounded device-side wait expired (see alibi_check_error) */
+    ALIBI_ERR_CHECK = -5        /* debug-checks build only: a kernel found a bad TMA / TMEM / shared
+                                   address, recorded it and skipped the access */
 } alibi_status;
 
 /* Library version as an integer (major * 10000 + minor * 100 + patch). */
@@ -335,7 +337,10 @@ ALIBI_API int alibi_selftest_fwd_timeout(const void *q, const void *k, const voi
  * Synchronise `stream`, then read and clear the device status word of the
  * current device. Returns ALIBI_ERR_TIMEOUT if a kernel gave up a bounded
  * wait since the last check, ALIBI_ERR_CUDA if the stream reports an error,
- * else ALIBI_OK. The word accumulates until it is collected here, but an
+ * ALIBI_ERR_CHECK if a kernel of the debug-checks build (the same library compiled
+ * with -DALIBI_CHECKS: every TMA coordinate, TMEM address and shared-memory operand
+ * tested before use) found a bad one (the second word of the status records the
+ * check and the value), else ALIBI_OK. The word accumulates until it is collected here, but an
  * uncollected error does not affect later calls: a kernel's waits give up early
  * only on a failure inside the same CTA, so calls made after a timeout compute
  * their results normally (the timeout is still reported by the next check).

@@ -53,7 +53,7 @@ def test_library_exports_nothing_undeclared(lib):
 
 def test_version_and_status_strings(lib):
     assert ab.alibi_version() >= 100
-    for s in (0, -1, -2, -3, -4):
+    for s in (0, -1, -2, -3, -4, -5):
         assert ab.alibi_status_str(s).startswith("ALIBI_")
 
 
