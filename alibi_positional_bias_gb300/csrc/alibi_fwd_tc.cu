@@ -78,31 +78,6 @@ struct Cfg {
     static constexpr uint32_t kSmem = kBar + 256 + 1024;   // barriers, TMEM slot, alignment slack
 };
 
-// Division by a runtime divisor d >= 1 of numerators below 2^31 as a multiply-high,
-// an add and a shift (Granlund and Montgomery, "Division by invariant integers using
-// multiplication", PLDI 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d)
-// + 1, n / d = (umulhi(n, m) + n) >> l. The work-item decoding runs it at every item
-// boundary, where a plain integer division is a long dependent sequence.
-struct FastDiv {
-    uint32_t d, m, l;
-};
-
-static FastDiv make_fastdiv(uint32_t d)
-{
-    uint32_t l = 0;
-    while ((1ull << l) < d) ++l;
-    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
-    return FastDiv{d, static_cast<uint32_t>(m), l};
-}
-
-__device__ __forceinline__ int fdiv(int n, const FastDiv &f)
-{
-    const uint32_t u = static_cast<uint32_t>(n);
-    return static_cast<int>((__umulhi(u, f.m) + u) >> f.l);
-}
-
-__device__ __forceinline__ int fmod_(int n, const FastDiv &f) { return n - fdiv(n, f) * static_cast<int>(f.d); }
-
 struct FwdParams {
     CUtensorMap tq, tk, tv;  // [BH, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
     CUtensorMap tout;        // [BH, N, d] bf16, box {32, 32, 1}, no swizzle (epilogue stores)
