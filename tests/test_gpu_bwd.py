@@ -3,25 +3,35 @@ oracle's gradients, which are pinned to finite differences of the forward.
 
 Tolerances. fp32 path: max-abs error <= 1e-5 x max(1, max |G|) per gradient
 tensor G (the 1e-5 of the forward, scaled to the gradient's magnitude). bf16
-tensor-core path: P and dS enter the tensor-core products rounded to bf16
-(relative 2^-9 each) and the results are rounded to bf16 (half an ulp, allowed
-on top); the largest term is D_i = dO_i . O_i taken from the forward's bf16
-output, whose rounding (2^-9 |dO_i| |O_i|) reaches every dS_ij of the row. When a
-row's weight sits on one key (steep heads) dP_ij - D_i cancels and that error is
-left alone: with N(0, 1) data at d <= 128 it reaches ~2^-6 of the gradient
-scale, so the test allows 2^-5 x max(1, max |G|) per (b, h).
+tensor-core path: a bound per element, derived from where the kernels round
+(gpu_helpers.bf16_grad_bounds): P^T enters dV += P^T dO and dS enters dQ and dK
+rounded to bf16 (unit roundoff 2^-8), and D_i = dO_i . O_i is taken from the
+forward's bf16 output, which is off by half an ulp plus the forward's own P
+rounding. Each gradient element must lie within twice its bound plus half a bf16
+ulp (the result's own rounding). Measured on the GB300 over this file's cases:
+dQ and dK reach at most 0.26 of the bound, dV 0.96 (a key with a single
+contributing query, where P's rounding is the whole error). The identities at
+full size keep a coarse 5% bound.
 """
 import numpy as np
 import pytest
 
 import alibi_inputs as gen
 import oracle
-from gpu_helpers import assert_grad, dev, host64
+from gpu_helpers import assert_grad, assert_grad_bound, bf16_grad_bounds, dev, host64
 
 pytestmark = pytest.mark.gpu
 
 TOL_F32_REL = 1e-5
-TOL_BF16_REL = 2.0 ** -5
+
+
+def check_bf16(got, q, k, v, do, refs, causal=True, m=None, variant=0, c_clamp=-87.0, z_cap=50.0, what=("dq", "dk", "dv")):
+    """The tensor-core gradients against the oracle's within the derived per-element bounds."""
+    rq, rk, rv, _, rowdot = refs
+    E = bf16_grad_bounds(q, k, v, do, rowdot, causal=causal, m=m, variant=variant, c_clamp=c_clamp, z_cap=z_cap)
+    for g, r, e, name in zip(got, (rq, rk, rv), E, ("dq", "dk", "dv")):
+        if name in what:
+            assert_grad_bound(g, r, e, name)
 
 
 @pytest.fixture(scope="module")
@@ -71,22 +81,18 @@ def run_bf16(ab, q, k, v, do, causal=True, slopes=None):
                                      (2, 2, 300, 64), (1, 4, 513, 128), (1, 2, 1000, 128)])
 def test_bwd_bf16_vs_oracle(ab, B, H, N, d, causal):
     q, k, v, do = cases(21 + N + d, B, H, N, d, "bf16")
-    dq, dk, dv = run_bf16(ab, q, k, v, do, causal)
-    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal)
-    check_grad(dq, rq, TOL_BF16_REL, "dq", bf16=True)
-    check_grad(dk, rk, TOL_BF16_REL, "dk", bf16=True)
-    check_grad(dv, rv, TOL_BF16_REL, "dv", bf16=True)
+    got = run_bf16(ab, q, k, v, do, causal)
+    refs = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal)
+    check_bf16(got, q.f32, k.f32, v.f32, do.f32, refs, causal=causal)
 
 
 def test_bwd_bf16_explicit_slopes(ab):
     H, N, d = 9, 600, 64
     m = ab.alibi_slopes_explicit(H, 16, 4096)
     q, k, v, do = cases(31, 1, H, N, d, "bf16")
-    dq, dk, dv = run_bf16(ab, q, k, v, do, slopes=m)
-    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, m=m.astype(np.float64))
-    check_grad(dq, rq, TOL_BF16_REL, "dq", bf16=True)
-    check_grad(dk, rk, TOL_BF16_REL, "dk", bf16=True)
-    check_grad(dv, rv, TOL_BF16_REL, "dv", bf16=True)
+    got = run_bf16(ab, q, k, v, do, slopes=m)
+    refs = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, m=m.astype(np.float64))
+    check_bf16(got, q.f32, k.f32, v.f32, do.f32, refs, m=m.astype(np.float64))
 
 
 def test_bwd_identities_at_layer_size(ab):
@@ -104,10 +110,8 @@ def test_bwd_identities_at_layer_size(ab):
     h = 5
     sl = (slice(0, 1), slice(h, h + 1))
     m = oracle.slopes(w.H)[h:h + 1]
-    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], m=m)
-    check_grad(dq[sl], rq, TOL_BF16_REL, "dq", bf16=True)
-    check_grad(dk[sl], rk, TOL_BF16_REL, "dk", bf16=True)
-    check_grad(dv[sl], rv, TOL_BF16_REL, "dv", bf16=True)
+    refs = oracle.attention_bwd(q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], m=m)
+    check_bf16((dq[sl], dk[sl], dv[sl]), q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], refs, m=m)
 
 
 def test_bwd_deterministic(ab):
@@ -160,11 +164,10 @@ def test_bwd_mitigations(ab, combo, d, causal):
     out, lse = ab.alibi_attn_fwd_ex(qd, kd, vd, causal=causal, **kw)
     dq, dk, dv = ab.alibi_attn_bwd(qd, kd, vd, out, lse, dod, causal=causal, **kw)
     ab.alibi_check_error()
-    rq, rk, rv, _, _ = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal,
-                                            variant=sum(ORC[c] for c in combo), c_clamp=-3.0, z_cap=8.0)
-    check_grad(host64(dq), rq, TOL_BF16_REL, "dq", bf16=True)
-    check_grad(host64(dk), rk, TOL_BF16_REL, "dk", bf16=True)
-    check_grad(host64(dv), rv, TOL_BF16_REL, "dv", bf16=True)
+    variant = sum(ORC[c] for c in combo)
+    refs = oracle.attention_bwd(q.f32, k.f32, v.f32, do.f32, causal=causal, variant=variant, c_clamp=-3.0, z_cap=8.0)
+    check_bf16((host64(dq), host64(dk), host64(dv)), q.f32, k.f32, v.f32, do.f32, refs, causal=causal,
+               variant=variant, c_clamp=-3.0, z_cap=8.0)
     if "softcap" in combo:
         # the cap's derivative is not vacuous on these inputs: 1 - tanh^2(A / z) is far from 1
         a = q.f32[0, 0].astype(np.float64) @ k.f32[0, 0].astype(np.float64).T / np.sqrt(d)
@@ -188,5 +191,5 @@ def test_bwd_long_context_prefix_rows_and_identities(ab):
     for h in (0, 7, 15):  # the shallowest, a middle and the steepest head
         sl = (slice(0, 1), slice(h, h + 1), slice(0, n))
         m = oracle.slopes(w.H)[h:h + 1]
-        rq, _, _, _, _ = oracle.attention_bwd(q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], m=m)
-        check_grad(dq[sl], rq, TOL_BF16_REL, "dq", bf16=True)
+        refs = oracle.attention_bwd(q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], m=m)
+        check_bf16((dq[sl], None, None), q.f32[sl], k.f32[sl], v.f32[sl], do.f32[sl], refs, m=m, what=("dq",))
