@@ -12,8 +12,10 @@
 // example that a production kernel generates the biases inside its tiles.
 //
 // Design (one persistent CTA per SM, 384 threads):
-//   warp 0      TMA producer: Q tiles once per work item, K/V tiles through
-//               two 2-stage rings (128-byte swizzle, zero fill past N).
+//   warp 0      TMA producer: Q tiles once per work item, K/V tiles through a
+//               2-stage ring of units, each K(u) with V(u-1) behind one barrier
+//               pair (128-byte swizzle, zero fill past N), so the MMA issuer
+//               tests one barrier and commits one release per KV tile.
 //   warp 1      TMEM allocator and MMA issuer (converged, one elected lane
 //               issues):
 //                 S_s = Q_s K^T   (128 x 128, fp32 in TMEM, smem x smem)
@@ -213,10 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBar);
     uint64_t *q_full = bars + 0;    // [2]
     uint64_t *q_empty = bars + 2;   // [1]
-    uint64_t *k_full = bars + 3;    // [2]
-    uint64_t *k_empty = bars + 5;   // [2]
-    uint64_t *v_full = bars + 7;    // [2]
-    uint64_t *v_empty = bars + 9;   // [2]
+    uint64_t *k_full = bars + 3;    // [2] ring unit of stage s loaded (K(u) and V(u - 1))
+    uint64_t *k_empty = bars + 5;   // [2] ring unit of stage s read by the MMAs
     uint64_t *s_full = bars + 11;   // [2]
     uint64_t *p_full = bars + 13;   // [2]
     uint64_t *o_full = bars + 15;   // [2]
@@ -237,8 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             mbar_init(&q_full[s], 1);
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 4);   // one arrival per softmax warp
             mbar_init(&p_hi[s], 4);
@@ -276,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t kc = 0, vc = 0;
+            uint32_t uc = 0;       // ring units issued
             int qk[2] = {-1, -1};  // item whose Q tile s was issued last
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -293,34 +291,32 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         tma_load_3d(smem + C::kQ + s * C::kTileBytes + c * C::kChunkBytes, &p.tq, 64 * c,
                                     (2 * t.qb + s) * BM, t.bh, &q_full[s]);
                 }
-                auto load_kv = [&](const CUtensorMap *map, uint32_t base, uint64_t *full, uint64_t *empty,
-                                   uint32_t &cnt, int jtile, uint32_t site) -> bool {
-                    const uint32_t st = cnt % 2, ph = (cnt / 2) & 1;
-                    if (!mbar_wait(&empty[st], ph ^ 1, err, site)) return false;
-                    mbar_arrive_expect_tx(&full[st], C::kTileBytes);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(smem + base + st * C::kTileBytes + c * C::kChunkBytes, map, 64 * c, jtile * BN,
-                                    t.bh, &full[st]);
-                    ++cnt;
-                    return true;
-                };
-                // order: K(0), K(1), V(0), K(2), V(1), ..., V(n-1)
-                for (int it = 0; it < t.n && ok; ++it) {
-                    ok = load_kv(&p.tk, C::kK, k_full, k_empty, kc, kv_tile(p, t, it), SITE_PROD_K);
-                    if (ok && it >= 1)
-                        ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, kv_tile(p, t, it - 1), SITE_PROD_V);
+                // One ring unit per step u = 0 .. n: K(u) (u < n) and V(u - 1) (u >= 1) into the
+                // K and V buffers of stage uc % 2, behind one barrier pair. Unit u is consumed
+                // in the MMA issuer's iteration u - 1 (P V of V(u-1), then S of K(u)).
+                for (int u = 0; u <= t.n && ok; ++u) {
+                    const uint32_t st = uc % 2, ph = (uc / 2) & 1;
+                    ok = mbar_wait(&k_empty[st], ph ^ 1, err, SITE_PROD_K);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&k_full[st], (u < t.n ? C::kTileBytes : 0u) + (u >= 1 ? C::kTileBytes : 0u));
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        if (u < t.n)
+                            tma_load_3d(smem + C::kK + st * C::kTileBytes + c * C::kChunkBytes, &p.tk, 64 * c,
+                                        kv_tile(p, t, u) * BN, t.bh, &k_full[st]);
+                        if (u >= 1)
+                            tma_load_3d(smem + C::kV + st * C::kTileBytes + c * C::kChunkBytes, &p.tv, 64 * c,
+                                        kv_tile(p, t, u - 1) * BN, t.bh, &k_full[st]);
+                    }
+                    ++uc;
                 }
-                if (ok) ok = load_kv(&p.tv, C::kV, v_full, v_empty, vc, kv_tile(p, t, t.n - 1), SITE_PROD_V);
             }
             // Drain (also after an error): the last load into each Q slot and ring stage
             // has landed before the CTA can exit. Earlier loads into a stage were consumed,
             // hence complete, before the stage was reused.
             for (int s = 0; s < 2; ++s)
                 if (qk[s] >= 0) mbar_wait(&q_full[s], qk[s] & 1, err, SITE_PROD_Q, true);
-            for (uint32_t n = kc > 2 ? kc - 2 : 0; n < kc; ++n)
+            for (uint32_t n = uc > 2 ? uc - 2 : 0; n < uc; ++n)
                 mbar_wait(&k_full[n % 2], (n / 2) & 1, err, SITE_PROD_K, true);
-            for (uint32_t n = vc > 2 ? vc - 2 : 0; n < vc; ++n)
-                mbar_wait(&v_full[n % 2], (n / 2) & 1, err, SITE_PROD_V, true);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -334,14 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
             const uint32_t sV = smem_u32(smem + C::kV);
             const bool aux = use_aux_bias(p, VAR);
             const uint64_t auxd = smem_desc_sw128(smem_u32(smem + C::kAux), 16, 1024);
-            uint32_t kc = 0, vc = 0;
+            uint32_t uc = 0;  // ring units consumed
             uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
                 if (w >= p.num_items) break;
                 const Item t = decode_item(p, w, CAUSAL);
-                const int last_slot = t.q1valid ? 1 : 0;
                 ok = mbar_wait(&q_full[0], k & 1, err, SITE_MMA_Q) && mbar_wait(&q_full[1], k & 1, err, SITE_MMA_Q);
                 if (ok && aux) ok = mbar_wait(&bias_full[k & 1], (k >> 1) & 1, err, SITE_MMA_Q);
                 ok = __all_sync(0xffffffffu, ok);
@@ -386,27 +381,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 bool first_pv[2] = {true, true};
                 // prologue: K(0) and the S of slots active at it = 0
                 {
-                    const uint32_t st = kc % 2, ph = (kc / 2) & 1;
+                    const uint32_t st = uc % 2, ph = (uc / 2) & 1;  // unit 0: K(0)
                     ok = mbar_wait(&k_full[st], ph, err, SITE_MMA_K);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     for (int s = 0; s < 2; ++s)
                         if (slot_active(t, s, 0, CAUSAL)) issue_S(s, st, kv_tile(p, t, 0));
                     mma_commit_w(&k_empty[st]);
+                    ++uc;
                 }
                 for (int it = 0; it < t.n && ok; ++it) {
-                    const uint32_t vst = (vc + it) % 2, vph = ((vc + it) / 2) & 1;
-                    ok = mbar_wait(&v_full[vst], vph, err, SITE_MMA_V);
+                    // unit it + 1: V(it) and K(it + 1), normally resident long before needed
+                    const uint32_t vst = uc % 2, uph = (uc / 2) & 1;
+                    ok = mbar_wait(&k_full[vst], uph, err, SITE_MMA_V);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
-                    // the next K tile is normally resident long before it is needed: wait
-                    // for it here, off the P -> PV -> S critical path
-                    if (it + 1 < t.n) {
-                        const uint32_t kst = (kc + it + 1) % 2, kph = ((kc + it + 1) / 2) & 1;
-                        ok = mbar_wait(&k_full[kst], kph, err, SITE_MMA_K);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                    }
                     for (int s = 0; s < 2 && ok; ++s) {
                         if (slot_active(t, s, it, CAUSAL)) {
                             ok = mbar_wait_spin(&p_full[s], p_cnt[s] & 1, err, SITE_MMA_P);
@@ -427,17 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                                 ++o_cnt[s];
                             }
                         }
-                        if (it + 1 < t.n && slot_active(t, s, it + 1, CAUSAL)) {
-                            const uint32_t kst = (kc + it + 1) % 2;
-                            issue_S(s, kst, kv_tile(p, t, it + 1));
-                            if (s == last_slot) mma_commit_w(&k_empty[kst]);
-                        }
+                        if (it + 1 < t.n && slot_active(t, s, it + 1, CAUSAL))
+                            issue_S(s, vst, kv_tile(p, t, it + 1));
                     }
-                    mma_commit_w(&v_empty[vst]);
+                    mma_commit_w(&k_empty[vst]);  // the unit's V and K have both been read
+                    ++uc;
                 }
                 mma_commit_w(q_empty);
-                kc += t.n;
-                vc += t.n;
             }
             // drain: every MMA issued above completes before TMEM is released
             mma_commit_w(mma_done);
