@@ -322,7 +322,7 @@ ALIBI_API int alibi_selftest_timeout(void *stream);
  * pages have no counterpart to it. Runs the bf16 prefill on the caller's buffers
  * (same arguments, layouts and checks as alibi_attn_fwd; the kernel build that
  * carries the mitigations, none of them enabled) with two changes: each CTA's TMA producer
- * leaves out the load of its first work item's first Q tile, and every bounded
+ * leaves out the loads of its first work item's Q tiles, and every bounded
  * wait gives up after wait_us microseconds (1 <= wait_us <= 1000000). The MMA
  * issuer's wait for that tile runs out; the kernel records ALIBI_ERR_TIMEOUT in
  * the device status word, its other roles stop at their next wait, every load

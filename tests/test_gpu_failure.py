@@ -32,8 +32,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_prefill_kernel_timeout_drains_and_context_survives(d):
-    # the prefill kernel's own failure path: every CTA's first Q tile is never
-    # loaded, the MMA issuer's wait for it runs out after 20 ms, the other roles
+    # the prefill kernel's own failure path: every CTA's first item's Q tiles are never
+    # loaded, the MMA issuer's wait for them runs out after 20 ms, the other roles
     # stop, the issued loads and MMAs are waited for and TMEM is freed
     import torch
     import alibi_positional_bias_gb300 as ab
