@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "alibi.h"
@@ -152,7 +153,13 @@ cudaMemPool_t decode_pool()
     return g_pool[dev];
 }
 
-void fill_slopes(int H, Slopes *s)
+// The schedule is evaluated in long double, which some hosts (Arm) emulate in
+// software at about half a microsecond per value, so each head count's table is
+// computed once per process and copied on later calls (the same values).
+namespace {
+std::atomic<const Slopes *> g_slope_cache[kMaxHeads + 1];
+
+void compute_slopes(int H, Slopes *s)
 {
     for (int h = 0; h < H && h < kMaxHeads; ++h) {
         int num, den;
@@ -160,6 +167,26 @@ void fill_slopes(int H, Slopes *s)
         s->nat[h] = slope_value(num, den);
         s->log2e[h] = static_cast<float>(static_cast<double>(s->nat[h]) * 1.4426950408889634);
     }
+}
+}  // namespace
+
+void fill_slopes(int H, Slopes *s)
+{
+    if (H < 1 || H > kMaxHeads) return compute_slopes(H, s);
+    const Slopes *c = g_slope_cache[H].load(std::memory_order_acquire);
+    if (!c) {
+        Slopes *fresh = new Slopes;
+        compute_slopes(H, fresh);
+        const Slopes *expected = nullptr;
+        if (g_slope_cache[H].compare_exchange_strong(expected, fresh, std::memory_order_acq_rel)) {
+            c = fresh;
+        } else {  // another thread published the same table first
+            delete fresh;
+            c = expected;
+        }
+    }
+    std::memcpy(s->nat, c->nat, sizeof(float) * static_cast<size_t>(H));
+    std::memcpy(s->log2e, c->log2e, sizeof(float) * static_cast<size_t>(H));
 }
 
 void fill_slopes_from(int H, const float *nat, Slopes *s)
