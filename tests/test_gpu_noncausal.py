@@ -39,12 +39,14 @@ def test_noncausal_shape_sweep(ab, B, H, N, d):
     assert_close(lse, rl, TOL_BF16_LSE, "lse")
 
 
-@pytest.mark.parametrize("name", ["heads6_n1024", "layer_n2048"])
+@pytest.mark.parametrize("name", ["heads6_n1024", "layer_n2048", "long_n16384"])
 def test_noncausal_workloads_sampled_rows(ab, name):
+    # rows of every (b, h): tile edges, the ragged tail, the last row, random rows
     w = gen.WORKLOADS[name]
     q, k, v = gen.generate(w)
     out, lse = run_bf16(ab, q, k, v)
-    rows = sample_rows(w.B, w.H, w.N, max_heads=8, per_head=16)
+    rows = sample_rows(w.B, w.H, w.N, max_heads=w.B * w.H, per_head=8 if w.N > 4096 else 16, seed=w.N + 1)
+    assert len(np.unique(rows // w.N)) == w.B * w.H
     ro, rl, _ = oracle.attention(q.f32, k.f32, v.f32, causal=False, rows=rows)
     assert_bf16_out(out.reshape(-1, w.d)[rows], ro)
     assert_close(lse.reshape(-1)[rows], rl, TOL_BF16_LSE, "lse")
