@@ -162,3 +162,46 @@ def test_peaked_weights_with_normal_values(ab, seed, B, H, N, d, sq):
     from gpu_helpers import half_ulp_bf16
     before_store = np.abs(out - ro) - half_ulp_bf16(ro)
     assert before_store.max() <= 2.0 ** -8 * np.abs(v.f32).max()
+
+
+def test_concurrent_host_threads(ab):
+    # Several host threads call the prefill at once, each on its own stream and with
+    # its own head count, so the per-device kernel set-up and the per-head-count slope
+    # tables are first created concurrently (the C calls run without the GIL). Every
+    # result must equal the same call made alone.
+    import threading
+    import torch
+    shapes = [(1, h, 300 + 17 * i, 128 if i % 2 else 64) for i, h in enumerate((3, 5, 7, 9, 11, 13))]
+    inputs = []
+    for i, (B, H, N, d) in enumerate(shapes):
+        q, k, v = gen.random_case(500 + i, B, H, N, d, dtype="bf16")
+        inputs.append(tuple(dev(t, "bf16") for t in (q, k, v)))
+    results = [None] * len(shapes)
+    errors = []
+    start = threading.Barrier(len(shapes))
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            start.wait()
+            for causal in (True, False):
+                with torch.cuda.stream(s):
+                    out, lse = ab.alibi_attn_fwd(*inputs[i], causal=causal, stream=s)
+                s.synchronize()
+                results[i] = results[i] or {}
+                results[i][causal] = (out, lse)
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(shapes))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    ab.alibi_check_error()
+    assert not errors, errors
+    for i in range(len(shapes)):
+        for causal in (True, False):
+            out, lse = ab.alibi_attn_fwd(*inputs[i], causal=causal)
+            ab.alibi_check_error()
+            assert torch.equal(out, results[i][causal][0]) and torch.equal(lse, results[i][causal][1]), (i, causal)
