@@ -203,6 +203,35 @@ def oracle_decode_sample(w, budget_s: float, seed: int = 1):
     return nbytes, secs, heads, threads
 
 
+def oracle_other_configs(budget_s: float) -> dict:
+    """The fp64 oracle on the other workloads, each a bounded sample in its own
+    metric's units (prefill GFLOP/s at the causal count, decode KV GB/s)."""
+    import numpy as np
+    import alibi_inputs as gen
+    import oracle
+    out = {}
+    # the tiny fp32 workload: the whole problem, repeated
+    w = gen.WORKLOADS["tiny_fp32"]
+    q, k, v = gen.generate(w)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        oracle.attention(q.f32, k.f32, v.f32, want_weights=True)
+        n += 1
+    secs = time.perf_counter() - t0
+    out["tiny_fp32"] = {"value": n * prefill_flops(w) / secs / 1e9, "unit": "GFLOP/s",
+                        "sample": f"the whole problem (weights included) {n} times, {secs:.1f} s"}
+    for name in ("heads6_n1024", "layer_n2048"):
+        w = gen.WORKLOADS[name]
+        f, secs, rows, _ = oracle_prefill_sample(w, budget_s, seed=7)
+        out[name] = {"value": f / secs / 1e9, "unit": "GFLOP/s",
+                     "sample": f"{rows} query rows of one head, {secs:.1f} s"}
+    w = gen.WORKLOADS[DECODE]
+    nbytes, secs, heads, _ = oracle_decode_sample(w, budget_s)
+    out[DECODE] = {"value": nbytes / secs / 1e9, "unit": "GB/s",
+                   "sample": f"{heads} (b, h) decode rows over their whole cache, {secs:.1f} s"}
+    return out
+
+
 def run_reference(args):
     """The reference arm: the fp64 CPU oracle, timed as it stands on the host cores."""
     import alibi_inputs as gen
@@ -663,7 +692,8 @@ def run_native(args):
         f, s, rows, threads = oracle_prefill_sample(wp, args.cpu_seconds)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(), "kind": "oracle",
                "sample": f"{rows} query rows of one head of {PREFILL} (causal FLOPs 4 (i+1) d per row), "
-                         f"fp64, {s:.1f} s"}
+                         f"fp64, {s:.1f} s",
+               "per_config": oracle_other_configs(args.cpu_seconds / 6.0)}
 
     if rank != 0:
         if world > 1:
