@@ -67,8 +67,8 @@ struct Cfg {
     static constexpr uint32_t kChunkBytes = BM * 128;      // one 64-column box: 16 KB
     static constexpr uint32_t kTileBytes = BM * D * 2;     // one 128 x D bf16 tile
     static constexpr uint32_t kQ = 0;                      // 2 Q tiles
-    static constexpr uint32_t kK = 2 * kTileBytes;         // K ring
-    static constexpr uint32_t kV = kK + kKStages * kTileBytes;  // V ring
+    static constexpr uint32_t kK = 2 * kTileBytes;         // K tiles of the two ring stages
+    static constexpr uint32_t kV = kK + kKStages * kTileBytes;  // V tiles of the two ring stages
     // One 128 x 64 swizzle atom of bias operands: ones (K-step 0, the A side), the
     // column bias m log2(e) c / c1 for the two items in flight (K-steps 1, 2, the B
     // side), and minus ones (K-step 3, the A side that turns the same column bias
@@ -215,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBar);
     uint64_t *q_full = bars + 0;    // [1] both Q tiles of the item loaded
     uint64_t *q_empty = bars + 2;   // [1]
-    uint64_t *k_full = bars + 3;    // [2] ring unit of stage s loaded (K(u) and V(u - 1))
-    uint64_t *k_empty = bars + 5;   // [2] ring unit of stage s read by the MMAs
+    uint64_t *unit_full = bars + 3;    // [2] ring unit of stage s loaded (K(u) and V(u - 1))
+    uint64_t *unit_empty = bars + 5;   // [2] ring unit of stage s read by the MMAs
     uint64_t *s_full = bars + 11;   // [2]
     uint64_t *p_full = bars + 13;   // [2]
     uint64_t *o_full = bars + 15;   // [2]
@@ -234,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         cta_err_init(p.wait_ns);
         cta_check_init(p.err, smem_raw, C::kSmem);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&unit_full[s], 1);
+            mbar_init(&unit_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 4);   // one arrival per softmax warp
             mbar_init(&p_hi[s], 4);
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t uc = 0;       // ring units issued
-            int qk[2] = {-1, -1};  // item whose Q tile s was issued last
+            int qk = -1;           // item whose Q tiles were issued last
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int w = item_index(k);
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // both Q tiles of the item behind one barrier (the failure-path self-test
                 // leaves out the first item's Q: the issuer's wait for it runs out)
                 if (!(VAR && p.test_skip_q0 && k == 0)) {
-                    qk[0] = k;
+                    qk = k;
                     mbar_arrive_expect_tx(&q_full[0], 2 * C::kTileBytes);
                     for (int s = 0; s < 2; ++s)
                         for (int c = 0; c < C::kChunks; ++c)
@@ -298,26 +298,26 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // in the MMA issuer's iteration u - 1 (P V of V(u-1), then S of K(u)).
                 for (int u = 0; u <= t.n && ok; ++u) {
                     const uint32_t st = uc % 2, ph = (uc / 2) & 1;
-                    ok = mbar_wait(&k_empty[st], ph ^ 1, err, SITE_PROD_K);
+                    ok = mbar_wait(&unit_empty[st], ph ^ 1, err, SITE_PROD_K);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(&k_full[st], (u < t.n ? C::kTileBytes : 0u) + (u >= 1 ? C::kTileBytes : 0u));
+                    mbar_arrive_expect_tx(&unit_full[st], (u < t.n ? C::kTileBytes : 0u) + (u >= 1 ? C::kTileBytes : 0u));
                     for (int c = 0; c < C::kChunks; ++c) {
                         if (u < t.n)
                             tma_load_3d(smem + C::kK + st * C::kTileBytes + c * C::kChunkBytes, &p.tk, 64 * c,
-                                        kv_tile(p, t, u) * BN, t.bh, &k_full[st]);
+                                        kv_tile(p, t, u) * BN, t.bh, &unit_full[st]);
                         if (u >= 1)
                             tma_load_3d(smem + C::kV + st * C::kTileBytes + c * C::kChunkBytes, &p.tv, 64 * c,
-                                        kv_tile(p, t, u - 1) * BN, t.bh, &k_full[st]);
+                                        kv_tile(p, t, u - 1) * BN, t.bh, &unit_full[st]);
                     }
                     ++uc;
                 }
             }
-            // Drain (also after an error): the last load into each Q slot and ring stage
+            // Drain (also after an error): the last Q load and the last load into each ring stage
             // has landed before the CTA can exit. Earlier loads into a stage were consumed,
             // hence complete, before the stage was reused.
-            if (qk[0] >= 0) mbar_wait(&q_full[0], qk[0] & 1, err, SITE_PROD_Q, true);
+            if (qk >= 0) mbar_wait(&q_full[0], qk & 1, err, SITE_PROD_Q, true);
             for (uint32_t n = uc > 2 ? uc - 2 : 0; n < uc; ++n)
-                mbar_wait(&k_full[n % 2], (n / 2) & 1, err, SITE_PROD_K, true);
+                mbar_wait(&unit_full[n % 2], (n / 2) & 1, err, SITE_PROD_K, true);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -383,18 +383,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                 // prologue: K(0) and the S of slots active at it = 0
                 {
                     const uint32_t st = uc % 2, ph = (uc / 2) & 1;  // unit 0: K(0)
-                    ok = mbar_wait(&k_full[st], ph, err, SITE_MMA_K);
+                    ok = mbar_wait(&unit_full[st], ph, err, SITE_MMA_K);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     for (int s = 0; s < 2; ++s)
                         if (slot_active(t, s, 0, CAUSAL)) issue_S(s, st, kv_tile(p, t, 0));
-                    mma_commit_w(&k_empty[st]);
+                    mma_commit_w(&unit_empty[st]);
                     ++uc;
                 }
                 for (int it = 0; it < t.n && ok; ++it) {
                     // unit it + 1: V(it) and K(it + 1), normally resident long before needed
                     const uint32_t vst = uc % 2, uph = (uc / 2) & 1;
-                    ok = mbar_wait(&k_full[vst], uph, err, SITE_MMA_V);
+                    ok = mbar_wait(&unit_full[vst], uph, err, SITE_MMA_V);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     for (int s = 0; s < 2 && ok; ++s) {
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const __grid_consta
                         if (it + 1 < t.n && slot_active(t, s, it + 1, CAUSAL))
                             issue_S(s, vst, kv_tile(p, t, it + 1));
                     }
-                    mma_commit_w(&k_empty[vst]);  // the unit's V and K have both been read
+                    mma_commit_w(&unit_empty[vst]);  // the unit's V and K have both been read
                     ++uc;
                 }
                 mma_commit_w(q_empty);
