@@ -30,6 +30,7 @@ __all__ = [
 
 ALIBI_OK, ALIBI_ERR_INVALID, ALIBI_ERR_UNSUPPORTED, ALIBI_ERR_CUDA, ALIBI_ERR_TIMEOUT, ALIBI_ERR_CHECK = 0, -1, -2, -3, -4, -5
 ALIBI_FWD_SKIP_UNDERFLOW, ALIBI_FWD_CLAMP, ALIBI_FWD_LOGDIST, ALIBI_FWD_SOFTCAP = 1, 2, 4, 8
+ALIBI_FWD_NOMINAL_ORDER = 16
 
 _lock = threading.Lock()
 _lib = None

@@ -88,6 +88,7 @@ struct BwdParams {
     __nv_bfloat16 *g0, *g1;       // dKdV: dk, dv; dQ: dq
     uint32_t *err;
     int N, BH, H, NT, num_items, causal;
+    const int2 *order;  // optional work order: entry .x = b h * NT + tile; null = nominal order
     float c1;       // log2(e) / sqrt(d)
     float inv_sqrt_d;
     // mitigations (kFwdClamp / kFwdLogDist / kFwdSoftcap), constants in base-2 units as in the forward
@@ -151,15 +152,28 @@ struct BItem {
     int bh, tile, n;
 };
 
-// dKdV items: round r of the schedule is KV tile r of every (b, h) (causal: the
-// longest first, since tile jt meets NT - jt query tiles).
+// Item at position idx of an order table: (b h, tile).
+__device__ __forceinline__ void table_item(const BwdParams &p, int idx, BItem *it)
+{
+    const int e = p.order[idx].x;
+    it->bh = e / p.NT;
+    it->tile = e - it->bh * p.NT;
+}
+
+// dKdV items: round r of the nominal schedule is KV tile r of every (b, h) (causal:
+// the longest first, since tile jt meets NT - jt query tiles); an order table gives
+// the blocked order of large causal launches instead.
 __device__ __forceinline__ BItem dkdv_item(const BwdParams &p, int idx, bool causal)
 {
     BItem it;
-    const int round = idx / p.BH;
-    it.bh = idx - round * p.BH;
-    it.tile = round;
-    it.n = causal ? p.NT - round : p.NT;
+    if (p.order) {
+        table_item(p, idx, &it);
+    } else {
+        const int round = idx / p.BH;
+        it.bh = idx - round * p.BH;
+        it.tile = round;
+    }
+    it.n = causal ? p.NT - it.tile : p.NT;
     return it;
 }
 
@@ -169,13 +183,18 @@ __device__ __forceinline__ int dkdv_qtile(const BItem &t, int it, bool causal)
     return causal ? t.tile + it : it;
 }
 
-// dQ items: round r is query tile NT - 1 - r of every (b, h) (causal: longest first).
+// dQ items: round r of the nominal schedule is query tile NT - 1 - r of every
+// (b, h) (causal: longest first), or the order table's item.
 __device__ __forceinline__ BItem dq_item(const BwdParams &p, int idx, bool causal)
 {
     BItem it;
-    const int round = idx / p.BH;
-    it.bh = idx - round * p.BH;
-    it.tile = p.NT - 1 - round;
+    if (p.order) {
+        table_item(p, idx, &it);
+    } else {
+        const int round = idx / p.BH;
+        it.bh = idx - round * p.BH;
+        it.tile = p.NT - 1 - round;
+    }
     it.n = causal ? it.tile + 1 : p.NT;
     return it;
 }
@@ -1036,6 +1055,9 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     if (!encode_tmap_bf16_3d(&p.tg0, dk, D, N, BH, 16, 32, false) ||
         !encode_tmap_bf16_3d(&p.tg1, dv, D, N, BH, 16, 32, false))
         return cudaErrorInvalidValue;
+    // large causal launches take the blocked work order (same items, same results)
+    const bool blocked = causal && !(flags & kFwdNominalOrder);
+    p.order = blocked ? causal_work_order(OrderKind::BwdDkDv, p.BH, N, D, stream) : nullptr;
     if (causal)
         bwd_dkdv_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else
@@ -1044,6 +1066,7 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
     if (!encode_tmap_bf16_3d(&p.tg0, dq, D, N, BH, 16, 32, false)) return cudaErrorInvalidValue;
+    p.order = blocked ? causal_work_order(OrderKind::BwdDq, p.BH, N, D, stream) : nullptr;
     if (causal)
         bwd_dq_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else

@@ -746,9 +746,14 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out
                    : launch_fwd_tc_d<64, false>(q, k, v, out, lse, B, H, N, d, causal, slopes, plan, flags, clamp_min,
                                                 softcap_z, test_wait_ns, stream);
     };
-    if (!(flags & kFwdSkipUnderflow)) return run(nullptr);
-    // underflow skipping: the plan lives in a stream-ordered scratch buffer for this call
     const int NQT = (N + BM - 1) / BM, NQB = (NQT + 1) / 2;
+    if (!(flags & kFwdSkipUnderflow)) {
+        // dense: the nominal order, or for causal launches whose K and V exceed half the L2 the
+        // cached blocked order (same items, same results)
+        const bool blocked = causal && !(flags & kFwdNominalOrder) && test_wait_ns == 0;
+        return run(blocked ? causal_work_order(OrderKind::Prefill, B * H, N, d, stream) : nullptr);
+    }
+    // underflow skipping: the plan lives in a stream-ordered scratch buffer for this call
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, NQB), decode_pool(), stream);
     if (e != cudaSuccess) return e;

@@ -6,10 +6,13 @@
 #include <cstdint>
 #include <cstring>
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "alibi.h"
 #include "internal.h"
+#include "work_order.h"
 
 namespace alibi {
 
@@ -22,6 +25,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 uint32_t *g_status_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+int g_l2[kMaxDevices] = {};
 cudaMemPool_t g_pool[kMaxDevices] = {};
 
 int current_device()
@@ -107,6 +111,97 @@ int num_sms()
         g_sms[dev] = n;
     }
     return g_sms[dev];
+}
+
+int l2_bytes()
+{
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_l2[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n < 1) n = -1;
+        g_l2[dev] = n;
+    }
+    return g_l2[dev];
+}
+
+// Blocked work-order tables (work_order.h), one per (device, kind, B*H, N, grid),
+// built on the first launch of that shape and kept for the life of the process.
+// Shapes for which the nominal order is kept are remembered too (null entries).
+const int2 *causal_work_order(OrderKind kind, int BH, int N, int dr, cudaStream_t stream)
+{
+    constexpr size_t kMaxTables = 256;               // cached shapes, null entries included
+    constexpr size_t kMaxBytes = size_t(256) << 20;  // device memory held by the tables
+    constexpr int64_t kMaxItems = int64_t(1) << 24;
+    const int NQT = (N + 127) / 128;
+    // items per head: prefill blocks of two Q tiles, or the backward's single tiles
+    const int per_head = kind == OrderKind::Prefill ? (NQT + 1) / 2 : NQT;
+    const int64_t n = static_cast<int64_t>(BH) * per_head;
+    // only where the nominal order re-reads a head's streamed tiles (K and V, or Q
+    // and dO) from DRAM: B*H heads of them above half the L2 (the resident tiles,
+    // the outputs and the far half of the cache take the rest), and at most 16
+    // blocks of 256 rows per head (with 32 or more the blocked order measured up
+    // to 3% slower: a head's items are long enough that the nominal order reuses
+    // its tiles)
+    const int l2 = l2_bytes();
+    if (NQT < 2 || NQT > 32 || n > kMaxItems || l2 <= 0) return nullptr;
+    if (4.0 * BH * static_cast<double>(N) * dr <= 0.5 * static_cast<double>(l2)) return nullptr;
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    const int G = static_cast<int>(std::min<int64_t>(n, num_sms()));
+    using Key = std::tuple<int, int, int, int, int>;
+    static std::map<Key, int2 *> tables;
+    static size_t held_bytes = 0;
+    static std::mutex mu;
+    const Key key(dev, static_cast<int>(kind), BH, N, G);
+    std::lock_guard<std::mutex> g(mu);
+    const auto it = tables.find(key);
+    if (it != tables.end()) return it->second;
+    if (tables.size() >= kMaxTables) return nullptr;
+    // the table is built outside any stream capture (a captured launch of a new
+    // shape keeps the nominal order, with identical results)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    const std::vector<int64_t> sched = kind == OrderKind::Prefill ? order::choose(BH, per_head, NQT, G)
+                                                                  : order::choose_single(BH, per_head, G);
+    const size_t bytes = sched.size() * sizeof(int2);
+    if (sched.empty() || held_bytes + bytes > kMaxBytes) {
+        tables[key] = nullptr;
+        return nullptr;
+    }
+    // entries (b h * per_head + index, 0): the prefill's block index is the rank;
+    // the backward's rank r is query tile r (dQ) or KV tile NT-1-r (dK/dV)
+    std::vector<int2> h(sched.size());
+    for (size_t i = 0; i < sched.size(); ++i) {
+        const int64_t bh = sched[i] / per_head, r = sched[i] - bh * per_head;
+        const int64_t idx = kind == OrderKind::BwdDkDv ? per_head - 1 - r : r;
+        h[i] = make_int2(static_cast<int>(bh * per_head + idx), 0);
+    }
+    // upload on a private stream and wait for it, so the table is complete before
+    // any stream can launch with it; relaxed capture mode keeps another thread's
+    // capture from refusing these calls
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    int2 *d = nullptr;
+    cudaStream_t up = nullptr;
+    bool ok = cudaMalloc(&d, bytes) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaMemcpyAsync(d, h.data(), bytes, cudaMemcpyHostToDevice, up) == cudaSuccess &&
+              cudaStreamSynchronize(up) == cudaSuccess;
+    if (up) cudaStreamDestroy(up);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (!ok) {
+        if (d) cudaFree(d);
+        cudaGetLastError();  // a failed table only means the nominal order
+        return nullptr;
+    }
+    tables[key] = d;
+    held_bytes += bytes;
+    return d;
 }
 
 cudaError_t prepare_kernel(const void *func, int smem, uint32_t regs)
@@ -216,6 +311,11 @@ bool encode_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint
 
 using namespace alibi;
 
+static_assert(kFwdSkipUnderflow == ALIBI_FWD_SKIP_UNDERFLOW && kFwdClamp == ALIBI_FWD_CLAMP &&
+                  kFwdLogDist == ALIBI_FWD_LOGDIST && kFwdSoftcap == ALIBI_FWD_SOFTCAP &&
+                  kFwdNominalOrder == ALIBI_FWD_NOMINAL_ORDER,
+              "flag values of the C ABI");
+
 extern "C" {
 
 int alibi_version(void) { return 100; }
@@ -301,7 +401,8 @@ int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, fl
     if (st != ALIBI_OK) return st;
     if (causal != 0 && causal != 1) return ALIBI_ERR_INVALID;
     if (d != 16 && d != 32 && d != 64 && d != 128) return ALIBI_ERR_UNSUPPORTED;
-    const unsigned int known = ALIBI_FWD_SKIP_UNDERFLOW | ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP;
+    const unsigned int known =
+        ALIBI_FWD_SKIP_UNDERFLOW | ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP | ALIBI_FWD_NOMINAL_ORDER;
     if (flags & ~known) return ALIBI_ERR_INVALID;
     if ((flags & ALIBI_FWD_CLAMP) && !(clamp_min < 0.0f)) return ALIBI_ERR_INVALID;
     if ((flags & ALIBI_FWD_SOFTCAP) && !(softcap_z > 0.0f && std::isfinite(softcap_z))) return ALIBI_ERR_INVALID;
@@ -334,7 +435,8 @@ int alibi_attn_bwd(const void *q, const void *k, const void *v, const void *out,
     const alibi_fwd_options none = {0u, 0.0f, 0.0f, nullptr};
     if (!opt) opt = &none;
     const unsigned int mit = ALIBI_FWD_CLAMP | ALIBI_FWD_LOGDIST | ALIBI_FWD_SOFTCAP;
-    if (opt->flags & ~(mit | ALIBI_FWD_SKIP_UNDERFLOW)) return ALIBI_ERR_INVALID;
+    // ALIBI_FWD_NOMINAL_ORDER keeps the nominal work order of the backward's kernels too
+    if (opt->flags & ~(mit | ALIBI_FWD_SKIP_UNDERFLOW | ALIBI_FWD_NOMINAL_ORDER)) return ALIBI_ERR_INVALID;
     if (opt->flags & ALIBI_FWD_SKIP_UNDERFLOW) return ALIBI_ERR_UNSUPPORTED;
     if ((opt->flags & ALIBI_FWD_CLAMP) && !(opt->clamp_min < 0.0f)) return ALIBI_ERR_INVALID;
     if ((opt->flags & ALIBI_FWD_SOFTCAP) && !(opt->softcap_z > 0.0f && std::isfinite(opt->softcap_z)))

@@ -115,7 +115,7 @@ def test_fwd_ex_flags_and_plan_errors(lib):
     def f(H, d, causal, *opt):
         o, keep = _opt(*opt)
         return lib.alibi_attn_fwd_ex(P, P, P, P, P, 1, H, 8, d, causal, o, None)
-    assert f(1, 64, 1, 16) == ab.ALIBI_ERR_INVALID                      # unknown flag
+    assert f(1, 64, 1, 32) == ab.ALIBI_ERR_INVALID                      # unknown flag
     assert f(1, 48, 1, 1) == ab.ALIBI_ERR_UNSUPPORTED                   # head size
     assert f(1, 64, 1, 2, 1.0) == ab.ALIBI_ERR_INVALID                  # clamp >= 0
     assert f(1, 64, 1, 8, 0.0, -5.0) == ab.ALIBI_ERR_INVALID            # z <= 0
