@@ -1055,9 +1055,9 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     if (!encode_tmap_bf16_3d(&p.tg0, dk, D, N, BH, 16, 32, false) ||
         !encode_tmap_bf16_3d(&p.tg1, dv, D, N, BH, 16, 32, false))
         return cudaErrorInvalidValue;
-    // large causal launches take the blocked work order (same items, same results)
-    const bool blocked = causal && !(flags & kFwdNominalOrder);
-    p.order = blocked ? causal_work_order(OrderKind::BwdDkDv, p.BH, N, D, stream) : nullptr;
+    // large launches take the blocked work order (same items, same results)
+    const bool blocked = !(flags & kFwdNominalOrder);
+    p.order = blocked ? work_order(OrderKind::BwdDkDv, causal, p.BH, N, D, stream) : nullptr;
     if (causal)
         bwd_dkdv_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else
@@ -1066,7 +1066,7 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
     if (!encode_tmap_bf16_3d(&p.tg0, dq, D, N, BH, 16, 32, false)) return cudaErrorInvalidValue;
-    p.order = blocked ? causal_work_order(OrderKind::BwdDq, p.BH, N, D, stream) : nullptr;
+    p.order = blocked ? work_order(OrderKind::BwdDq, causal, p.BH, N, D, stream) : nullptr;
     if (causal)
         bwd_dq_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
     else

@@ -748,10 +748,10 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out
     };
     const int NQT = (N + BM - 1) / BM, NQB = (NQT + 1) / 2;
     if (!(flags & kFwdSkipUnderflow)) {
-        // dense: the nominal order, or for causal launches whose K and V exceed half the L2 the
+        // dense: the nominal order, or for launches whose K and V exceed half the L2 the
         // cached blocked order (same items, same results)
-        const bool blocked = causal && !(flags & kFwdNominalOrder) && test_wait_ns == 0;
-        return run(blocked ? causal_work_order(OrderKind::Prefill, B * H, N, d, stream) : nullptr);
+        const bool blocked = !(flags & kFwdNominalOrder) && test_wait_ns == 0;
+        return run(blocked ? work_order(OrderKind::Prefill, causal, B * H, N, d, stream) : nullptr);
     }
     // underflow skipping: the plan lives in a stream-ordered scratch buffer for this call
     void *ws = nullptr;

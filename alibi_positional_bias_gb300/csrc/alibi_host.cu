@@ -126,10 +126,11 @@ int l2_bytes()
     return g_l2[dev];
 }
 
-// Blocked work-order tables (work_order.h), one per (device, kind, B*H, N, grid),
-// built on the first launch of that shape and kept for the life of the process.
-// Shapes for which the nominal order is kept are remembered too (null entries).
-const int2 *causal_work_order(OrderKind kind, int BH, int N, int dr, cudaStream_t stream)
+// Blocked work-order tables (work_order.h), one per (device, kind, mask, B*H, N,
+// grid), built on the first launch of that shape and kept for the life of the
+// process. Shapes for which the nominal order is kept are remembered too (null
+// entries).
+const int2 *work_order(OrderKind kind, int causal, int BH, int N, int dr, cudaStream_t stream)
 {
     constexpr size_t kMaxTables = 256;               // cached shapes, null entries included
     constexpr size_t kMaxBytes = size_t(256) << 20;  // device memory held by the tables
@@ -150,11 +151,11 @@ const int2 *causal_work_order(OrderKind kind, int BH, int N, int dr, cudaStream_
     const int dev = current_device();
     if (dev < 0) return nullptr;
     const int G = static_cast<int>(std::min<int64_t>(n, num_sms()));
-    using Key = std::tuple<int, int, int, int, int>;
+    using Key = std::tuple<int, int, int, int, int, int>;
     static std::map<Key, int2 *> tables;
     static size_t held_bytes = 0;
     static std::mutex mu;
-    const Key key(dev, static_cast<int>(kind), BH, N, G);
+    const Key key(dev, static_cast<int>(kind), causal, BH, N, G);
     std::lock_guard<std::mutex> g(mu);
     const auto it = tables.find(key);
     if (it != tables.end()) return it->second;
@@ -166,8 +167,9 @@ const int2 *causal_work_order(OrderKind kind, int BH, int N, int dr, cudaStream_
         cudaGetLastError();
         return nullptr;
     }
-    const std::vector<int64_t> sched = kind == OrderKind::Prefill ? order::choose(BH, per_head, NQT, G)
-                                                                  : order::choose_single(BH, per_head, G);
+    const std::vector<int64_t> sched = !causal                      ? order::choose_uniform(BH, per_head, G)
+                                       : kind == OrderKind::Prefill ? order::choose(BH, per_head, NQT, G)
+                                                                    : order::choose_single(BH, per_head, G);
     const size_t bytes = sched.size() * sizeof(int2);
     if (sched.empty() || held_bytes + bytes > kMaxBytes) {
         tables[key] = nullptr;

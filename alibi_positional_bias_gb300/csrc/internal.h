@@ -30,13 +30,13 @@ void fill_slopes(int H, Slopes *s);
 void fill_slopes_from(int H, const float *nat, Slopes *s);  // caller-chosen slopes (natural-log units)
 int num_sms();                   // of the current device
 int l2_bytes();                  // L2 size of the current device
-// Blocked work order (work_order.h) of a dense causal launch over B*H heads of N
-// rows, head size dr: the prefill, or one of the backward's two kernels. A device
-// table of (item, 0) entries cached per device and shape, or null for the nominal
-// order (the streamed tiles fit in L2, the model prefers it, or the stream is
-// being captured before the shape's table exists).
+// Blocked work order (work_order.h) of a dense launch over B*H heads of N rows,
+// head size dr, causal or not: the prefill, or one of the backward's two kernels.
+// A device table of (item, 0) entries cached per device and shape, or null for
+// the nominal order (the streamed tiles fit in L2, the model prefers it, or the
+// stream is being captured before the shape's table exists).
 enum class OrderKind { Prefill = 0, BwdDkDv = 1, BwdDq = 2 };
-const int2 *causal_work_order(OrderKind kind, int BH, int N, int dr, cudaStream_t stream);
+const int2 *work_order(OrderKind kind, int causal, int BH, int N, int dr, cudaStream_t stream);
 // Once per (current device, kernel): check that `func` compiled to `regs` registers
 // per thread (0: any count) and raise its dynamic shared-memory limit to `smem`
 // bytes. Function attributes belong to each device's context, so a process that

@@ -1,5 +1,5 @@
-// Work order of dense causal launches (prefill and backward) whose streamed
-// tiles do not fit in L2.
+// Work order of dense launches (prefill and backward) whose streamed tiles do
+// not fit in L2.
 //
 // A prefill item is one (b, h) and one block qb of two 128-row Q tiles; a causal
 // item reads the KV tiles up to its diagonal, so its length grows with qb. The
@@ -26,7 +26,8 @@
 // A load model (the item's KV tiles plus a fixed cost per item) picks the better
 // of the two and falls back to the nominal order if neither is within 2% of its
 // balance. The backward's one-tile items (dK/dV per KV tile, dQ per query tile)
-// take the same construction, ranked by their length.
+// take the same construction, ranked by their length; without the causal mask
+// every item has the same length and the blocked order is taken as it is.
 //
 // Plain C++ (no CUDA types): the host builds the table once per shape, and the
 // tests compile this header with the host compiler.
@@ -128,6 +129,13 @@ inline std::vector<int64_t> choose_by(long BH, int NQB, Len len, long G, double 
 inline std::vector<int64_t> choose(long BH, int NQB, int NQT, long G)
 {
     return choose_by(BH, NQB, [NQT](int qb) { return item_tiles(qb, NQT); }, G, kItemCost);
+}
+
+// Items of equal length (the symmetric, non-causal bias: every item visits all
+// tiles): any order is as balanced as the nominal one, so the blocked order.
+inline std::vector<int64_t> choose_uniform(long BH, int per_head, long G)
+{
+    return choose_by(BH, per_head, [](int) { return 1; }, G, 0.0);
 }
 
 // The backward's schedule: NT one-tile items per head, ranked r = 0 .. NT-1 by

@@ -126,19 +126,20 @@ typedef struct alibi_fwd_options {
  * Goes Blind", sec. 3.4 (the paper trains with clamp_min = -87, sec. 4.3, and
  * z = 50), in any combination. They cannot be combined with
  * ALIBI_FWD_SKIP_UNDERFLOW (clamped or log-scaled biases do not underflow). *
- * Work order: a causal launch whose K and V (4 B H N d bytes) exceed half the
- * L2 cache and that has at most 16 blocks of 256 rows per head runs its work
- * items head by head in blocks of two rounds of the persistent grid, so each
- * head's K and V are read from DRAM about once; the first such launch of a
- * shape on a device builds a table of B H ceil(N/256) x 8 bytes in device
+ * Work order: a launch (causal or not) whose K and V (4 B H N d bytes) exceed
+ * half the L2 cache and that has at most 16 blocks of 256 rows per head runs
+ * its work items head by head in blocks of two rounds of the persistent grid,
+ * so each head's K and V are read from DRAM about once. The first such launch
+ * of a shape on a device builds a table of B H ceil(N/256) x 8 bytes in device
  * memory, which the library keeps for the life of the process (at most 256
  * shapes and 256 MiB; beyond that, and when the first launch of a shape is
  * made while its stream is being captured, the nominal order runs). Every
  * item computes the same values in either order: output and LSE are
  * bit-identical. ALIBI_FWD_NOMINAL_ORDER keeps the nominal longest-first order
  * (no table). alibi_attn_bwd applies the same rule to its two kernels (dK/dV
- * items stream a head's Q and dO, dQ items its K and V; one table each) and
- * honours the same flag; its gradients are bit-identical in either order too.
+ * items stream a head's Q and dO, dQ items its K and V; one table of
+ * B H ceil(N/128) x 8 bytes each) and honours the same flag; its gradients are
+ * bit-identical in either order too.
  */
 ALIBI_API int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse,
                    int B, int H, int N, int d, int causal, const alibi_fwd_options *opt, void *stream);

@@ -1,14 +1,15 @@
-"""Work order of dense causal launches whose streamed tiles exceed half the L2.
+"""Work order of dense launches whose streamed tiles exceed half the L2.
 
 Such launches (prefill, and the backward's dK/dV and dQ kernels) run their items
 in the blocked order (csrc/work_order.h) from tables the library builds once per
 shape. Every item computes the same values in either order, so output, LSE and
 gradients must be bit-identical to the nominal order (ALIBI_FWD_NOMINAL_ORDER),
-for the plain kernels, the mitigation kernels and the D = 64 kernels, on shapes
-that take the blocked order: several block counts per head, a ragged N with an
-odd number of tiles, and a launch made while its stream is being captured (which
-keeps the nominal order until the shape has a table). The ragged prefill is also
-checked against the oracle on sampled rows of every head."""
+for the plain kernels, the mitigation kernels and the D = 64 kernels, causal
+and not, on shapes that take the blocked order: several block counts per head,
+a ragged N with an odd number of tiles, and a launch made while its stream is
+being captured (which keeps the nominal order until the shape has a table). The
+ragged prefill is also checked against the oracle on sampled rows of every
+head."""
 import numpy as np
 import pytest
 
@@ -27,7 +28,8 @@ def ab():
 
 
 def blocked_regime(B, H, N, d):
-    # the library's rule: K and V above half the L2, at most 16 blocks of 256 rows per head
+    # the library's rule (causal or not): K and V above half the L2, at most 16
+    # blocks of 256 rows per head
     import torch
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     return 4 * B * H * N * d > l2 / 2 and 2 <= (N + 255) // 256 <= 16
@@ -56,6 +58,27 @@ def test_blocked_order_bit_identical(ab, B, H, N, d):
     o1, l1, o2, l2 = both_orders(ab, q, k, v)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert torch.isfinite(o1).all() and torch.isfinite(l1).all()
+
+
+@pytest.mark.parametrize("B,H,N,d", [(4, 32, 2048, 128), (16, 32, 1024, 64), (8, 20, 1900, 128)])
+def test_blocked_order_noncausal(ab, B, H, N, d):
+    # the symmetric bias over all keys: every item has the same length and the
+    # blocked order is taken as it is; forward and backward bit-identical
+    import torch
+    assert blocked_regime(B, H, N, d)
+    g = torch.Generator(device="cuda").manual_seed(B + H + N + d + 77)
+    q = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    k = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    v = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    do = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    o1, l1 = ab.alibi_attn_fwd_ex(q, k, v, causal=False)
+    o2, l2 = ab.alibi_attn_fwd_ex(q, k, v, causal=False, flags=ab.ALIBI_FWD_NOMINAL_ORDER)
+    g1 = ab.alibi_attn_bwd(q, k, v, o1, l1, do, causal=False)
+    g2 = ab.alibi_attn_bwd(q, k, v, o1, l1, do, causal=False, flags=ab.ALIBI_FWD_NOMINAL_ORDER)
+    ab.alibi_check_error()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for a, b, name in zip(g1, g2, ("dq", "dk", "dv")):
+        assert torch.equal(a, b), name
 
 
 def test_blocked_order_mitigation_kernel(ab):

@@ -13,8 +13,10 @@ shapes (ragged Q-tile counts, G = 1, G above the item count, odd NQB):
   fewest items a head keeps in the body (the locality the order exists for);
 * for whole-head blocks (nothing held back, NQB divides 2G) every CTA gets the
   same load over each complete block;
-* choose() never returns a schedule the load model puts more than 2% above the
-  nominal order, and returns the nominal order where ordering cannot matter.
+* choose() (prefill items) and choose_single() (the backward's one-tile items)
+  never return a schedule the load model puts more than 2% above the nominal
+  order, and return the nominal order where ordering cannot matter;
+  choose_uniform() (equal lengths, no causal mask) takes the blocked order.
 
 Plus the loads worked out by hand for one small case. No GPU involved."""
 import os
@@ -143,6 +145,29 @@ int main()
                         EXPECT(c == blocked(BH, NQB, G, false) || c == blocked(BH, NQB, G, true), "choose is one of the two");
                     }
                 }
+    // the backward's one-tile items (lengths r + 1) and equal-length items
+    for (long BH : {1L, 12L, 128L, 320L, 512L})
+        for (int NT : {1, 2, 5, 16, 31, 32})
+            for (long G0 : {5L, 152L}) {
+                const long n = BH * NT, G = std::min(n, G0);
+                const auto len1 = [](int r) { return r + 1; };
+                auto c = choose_single(BH, NT, G);
+                if (NT < 2 || n <= 2 * G) EXPECT(c.empty(), "single BH %ld NT %d G %ld", BH, NT, G);
+                if (!c.empty()) {
+                    check_schedule(c, BH, NT, 2 * NT, G, c == blocked(BH, NT, G, true) && c != blocked(BH, NT, G, false));
+                    EXPECT(makespan_by(c, BH, NT, len1, G, 1.0) <= 1.02 * makespan_by({}, BH, NT, len1, G, 1.0),
+                           "single balance BH %ld NT %d G %ld", BH, NT, G);
+                }
+                auto u = choose_uniform(BH, NT, G);
+                if (NT >= 2 && n > 2 * G) {
+                    EXPECT(u == blocked(BH, NT, G, false), "uniform BH %ld NT %d G %ld", BH, NT, G);
+                    // as balanced as the nominal order: item counts per CTA differ by at most one
+                    const auto one = [](int) { return 1; };
+                    EXPECT(makespan_by(u, BH, NT, one, G, 0.0) == makespan_by({}, BH, NT, one, G, 0.0), "uniform count");
+                } else {
+                    EXPECT(u.empty(), "uniform small BH %ld NT %d G %ld", BH, NT, G);
+                }
+            }
     // a decoder-layer launch (B = 4, H = 32, N = 2048: 128 heads x 8 blocks on 152 CTAs)
     // gets the blocked order with the nominal order's balance
     {
