@@ -24,6 +24,11 @@
  *   - stream is a cudaStream_t (NULL = the legacy default stream). Calls are
  *     asynchronous: results are valid once the stream has been synchronised.
  *   - scale is 1/sqrt(d); slopes are always those of alibi_slopes(H).
+ *   - The library keeps some state per device for the life of the process:
+ *     the device status word, a stream-ordered memory pool, kernel attributes
+ *     and the work-order tables of alibi_attn_fwd_ex. cudaDeviceReset() of a
+ *     device destroys that state with the context; do not call the library on
+ *     that device again in the same process after a reset.
  *   - Return value: ALIBI_OK, or a negative alibi_status. Argument errors are
  *     detected on the host before anything is launched. No call aborts the
  *     process, traps on the device or waits without bound: every device-side
