@@ -315,6 +315,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // D from the row-sum pre-pass is complete and visible from here on; the dQ
+    // kernel, which reads nothing this kernel writes, may then take each SM this
+    // grid's CTAs leave
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
@@ -970,6 +975,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // this grid may have started while the dK/dV kernel ran; it completes only after
+    // that kernel has, so stream order after the backward holds for both
+    griddep_wait();
 }
 
 // ---------------------------------------------------------------- D = dO . O
@@ -981,6 +989,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
                                                        float *__restrict__ dsum, long long rows)
 {
     constexpr int LPR = D / 8, RPW = 32 / LPR;
+    griddep_launch_dependents();  // the dK/dV kernel waits for this grid before it reads D
     const int lane = threadIdx.x & 31;
     const long long row = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW + lane / LPR;
     const int l = lane % LPR;
@@ -998,6 +1007,25 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
 #pragma unroll
     for (int o = LPR / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (row < rows && l == 0) dsum[row] = acc;
+}
+
+// Launch with programmatic stream serialization: the grid may start on SMs the
+// previous grid in the stream has left, before that grid has finished (the
+// kernels order their own dependences with griddep_wait).
+static cudaError_t launch_dependent(void (*kernel)(BwdParams), int grid, int smem, cudaStream_t stream,
+                                    const BwdParams &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <int D, bool VAR>
@@ -1058,20 +1086,15 @@ cudaError_t launch_bwd_d(const void *q, const void *k, const void *v, const void
     // large launches take the blocked work order (same items, same results)
     const bool blocked = !(flags & kFwdNominalOrder);
     p.order = blocked ? work_order(OrderKind::BwdDkDv, causal, p.BH, N, D, stream) : nullptr;
-    if (causal)
-        bwd_dkdv_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
-    else
-        bwd_dkdv_kernel<D, VAR, false><<<grid, kThreads, C::kSmem, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(causal ? bwd_dkdv_kernel<D, VAR, true> : bwd_dkdv_kernel<D, VAR, false>, grid, C::kSmem,
+                         stream, p);
+    if (e != cudaSuccess) return e;
     p.g0 = static_cast<__nv_bfloat16 *>(dq);
     p.g1 = nullptr;
     if (!encode_tmap_bf16_3d(&p.tg0, dq, D, N, BH, 16, 32, false)) return cudaErrorInvalidValue;
     p.order = blocked ? work_order(OrderKind::BwdDq, causal, p.BH, N, D, stream) : nullptr;
-    if (causal)
-        bwd_dq_kernel<D, VAR, true><<<grid, kThreads, C::kSmem, stream>>>(p);
-    else
-        bwd_dq_kernel<D, VAR, false><<<grid, kThreads, C::kSmem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(causal ? bwd_dq_kernel<D, VAR, true> : bwd_dq_kernel<D, VAR, false>, grid, C::kSmem,
+                            stream, p);
 }
 
 }  // namespace
