@@ -1,4 +1,4 @@
-"""The blocked work order of the dense causal prefill (csrc/work_order.h), on the host.
+"""The blocked work order of dense launches (csrc/work_order.h), on the host.
 
 The header is plain C++; a small program compiled with g++ checks, over a grid of
 shapes (ragged Q-tile counts, G = 1, G above the item count, odd NQB):
