@@ -167,3 +167,74 @@ def test_backward_blocked_order_bit_identical(ab, B, H, N, d, flags):
     for a, b, name in zip(g1, g2, ("dq", "dk", "dv")):
         assert torch.equal(a, b), name
         assert torch.isfinite(a).all(), name
+
+
+def test_blocked_order_from_concurrent_threads(ab):
+    # four host threads launch the same new shape (no table yet) on their own streams:
+    # one builds the table while the others wait for it; every result equals the
+    # nominal order's
+    import threading
+    import torch
+    B, H, N, d = 20, 16, 1024, 128   # a shape no other test launches
+    assert blocked_regime(B, H, N, d)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    q = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    k = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    v = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    ref_o, ref_l = ab.alibi_attn_fwd_ex(q, k, v, flags=ab.ALIBI_FWD_NOMINAL_ORDER)
+    torch.cuda.synchronize()
+    results, errors = [None] * 4, []
+
+    def worker(t):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                results[t] = ab.alibi_attn_fwd(q, k, v)
+            s.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    ab.alibi_check_error()
+    for o, l in results:
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+
+
+def test_backward_blocked_order_in_a_graph(ab):
+    # forward and backward of a blocked-order shape captured in a CUDA graph (the
+    # tables exist from a first call; the backward's kernels launch as programmatic
+    # dependents inside the graph) and replayed: equal to the direct calls
+    import torch
+    B, H, N, d = 4, 32, 2048, 128
+    assert blocked_regime(B, H, N, d)
+    g = torch.Generator(device="cuda").manual_seed(21)
+    q = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    k = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    v = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    do = torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16()
+    o_ref, l_ref = ab.alibi_attn_fwd(q, k, v)
+    g_ref = ab.alibi_attn_bwd(q, k, v, o_ref, l_ref, do)
+    torch.cuda.synchronize()
+    out, lse = torch.empty_like(q), torch.empty(B, H, N, device="cuda")
+    grads = [torch.empty_like(q) for _ in range(3)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        ab.alibi_attn_fwd(q, k, v, out=out, lse=lse)
+        ab.alibi_attn_bwd(q, k, v, out, lse, do, *grads)
+    for _ in range(2):
+        for t in (out, lse, *grads):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        ab.alibi_check_error()
+        assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
+        for a, b, name in zip(grads, g_ref, ("dq", "dk", "dv")):
+            assert torch.equal(a, b), name
