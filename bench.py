@@ -660,24 +660,29 @@ def run_native(args):
                "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
                "steps": ke, "pipelined": "uploads of step i+1 and downloads of step i-1 overlap step i's kernel"}
         # The same uploads and downloads with no kernel between them: the floor the
-        # host link sets on this loop, whatever the kernel's speed.
-        e0.record(stream)
-        up.wait_event(e0)
-        down.wait_event(e0)
-        for i in range(ke):
-            bq, bk, bv, bo, bl = dbufs[i % 2]
-            with torch.cuda.stream(up):
-                bq.copy_(hq, non_blocking=True)
-                bk.copy_(hk, non_blocking=True)
-                bv.copy_(hv, non_blocking=True)
-            with torch.cuda.stream(down):
-                hos[i % 2].copy_(bo, non_blocking=True)
-                hls[i % 2].copy_(bl, non_blocking=True)
-        stream.wait_stream(up)
-        stream.wait_stream(down)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        tc = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+        # host link sets on this loop, whatever the kernel's speed (the best of three
+        # runs: the host link of a shared box varies from run to run).
+        best = None
+        for _ in range(3):
+            e0.record(stream)
+            up.wait_event(e0)
+            down.wait_event(e0)
+            for i in range(ke):
+                bq, bk, bv, bo, bl = dbufs[i % 2]
+                with torch.cuda.stream(up):
+                    bq.copy_(hq, non_blocking=True)
+                    bk.copy_(hk, non_blocking=True)
+                    bv.copy_(hv, non_blocking=True)
+                with torch.cuda.stream(down):
+                    hos[i % 2].copy_(bo, non_blocking=True)
+                    hls[i % 2].copy_(bl, non_blocking=True)
+            stream.wait_stream(up)
+            stream.wait_stream(down)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        tc = torch.tensor([best], dtype=torch.float64, device=dev)
         if world > 1:
             dist.all_reduce(tc, op=dist.ReduceOp.MAX)
         e2e["ms_per_step"] = float(t[0]) / ke
