@@ -47,6 +47,8 @@ def both_orders(ab, q, k, v, flags=0, **kw):
     (16, 32, 1024, 128),   # 4 blocks per head, 512 heads
     (4, 32, 4096, 128),    # 16 blocks per head
     (16, 32, 1024, 64),    # the D = 64 kernel
+    (32, 32, 1024, 32),    # head size 32 on the D = 64 kernel
+    (64, 32, 1024, 16),    # head size 16 on the D = 64 kernel
 ])
 def test_blocked_order_bit_identical(ab, B, H, N, d):
     import torch
@@ -91,6 +93,11 @@ def test_blocked_order_mitigation_kernel(ab):
     o1, l1, o2, l2 = both_orders(ab, q, k, v, flags=ab.ALIBI_FWD_CLAMP | ab.ALIBI_FWD_SOFTCAP, clamp_min=-20.0,
                                  softcap_z=30.0)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # the symmetric bias with log-scaled distances
+    o1 = ab.alibi_attn_fwd_ex(q, k, v, causal=False, flags=ab.ALIBI_FWD_LOGDIST)
+    o2 = ab.alibi_attn_fwd_ex(q, k, v, causal=False, flags=ab.ALIBI_FWD_LOGDIST | ab.ALIBI_FWD_NOMINAL_ORDER)
+    ab.alibi_check_error()
+    assert torch.equal(o1[0], o2[0]) and torch.equal(o1[1], o2[1])
 
 
 def test_blocked_order_ragged_vs_oracle(ab):
