@@ -143,8 +143,8 @@ typedef struct alibi_fwd_options {
  * bit-identical. ALIBI_FWD_NOMINAL_ORDER keeps the nominal longest-first order
  * (no table). alibi_attn_bwd applies the same rule to its two kernels (dK/dV
  * items stream a head's Q and dO, dQ items its K and V; one table of
- * B H ceil(N/128) x 8 bytes each) and honours the same flag; its gradients are
- * bit-identical in either order too.
+ * B H ceil(N/128) x 8 bytes each), without the limit on blocks per head, and
+ * honours the same flag; its gradients are bit-identical in either order too.
  */
 ALIBI_API int alibi_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse,
                    int B, int H, int N, int d, int causal, const alibi_fwd_options *opt, void *stream);
