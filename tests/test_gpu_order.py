@@ -28,7 +28,7 @@ def ab():
 
 
 def blocked_regime(B, H, N, d):
-    # the library's rule (causal or not): K and V above half the L2, at most 16
+    # the prefill's rule (causal or not): K and V above half the L2, at most 16
     # blocks of 256 rows per head
     import torch
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
