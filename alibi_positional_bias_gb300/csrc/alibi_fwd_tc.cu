@@ -755,7 +755,7 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, void *out
     }
     // underflow skipping: the plan lives in a stream-ordered scratch buffer for this call
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, NQB), decode_pool(), stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, N), decode_pool(), stream);
     if (e != cudaSuccess) return e;
     int2 *plan = nullptr;
     e = launch_skip_plan(q, k, B, H, N, d, slopes, ws, &plan, nullptr, stream);

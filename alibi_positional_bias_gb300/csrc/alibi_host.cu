@@ -486,7 +486,7 @@ int alibi_attn_skip_plan(const void *q, const void *k, int B, int H, int N, int 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int NQB = ((N + 127) / 128 + 1) / 2, items = B * H * NQB;
     void *ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, NQB), decode_pool(), cs) != cudaSuccess)
+    if (cudaMallocFromPoolAsync(&ws, skip_plan_bytes(B * H, N), decode_pool(), cs) != cudaSuccess)
         return ALIBI_ERR_CUDA;
     int2 *info = nullptr;
     cudaError_t e = launch_skip_plan(q, k, B, H, N, d, s, ws, nullptr, &info, cs);

@@ -47,31 +47,62 @@ __device__ __forceinline__ void bf16x8(const uint4 &u, float (&f)[8])
     }
 }
 
-// Max squared key norm per (b, h): a one-dimensional grid of nblk 256-key blocks per
-// (b, h) (so B*H may exceed the 65535 limit of a second grid dimension), 256
-// threads, LPK lanes per key.
+// Max squared key norm per (b, h), and per row i of the same pass |q_i|^2 and
+// q_i.k_i (query and key rows share the index): a one-dimensional grid of nblk
+// 256-row blocks per (b, h) (so B*H may exceed the 65535 limit of a second grid
+// dimension), 256 threads, LPK lanes per row, four rows of each lane group in
+// flight. rows[bh N + i] = (|q_i|^2, q_i.k_i), each sum in the same order as the
+// per-row sums the plan needs, so the plan reads 8 bytes per row instead of Q and K.
 template <int D>
-__global__ void __launch_bounds__(256) kmax_kernel(const __nv_bfloat16 *__restrict__ k, int N, int nblk,
-                                                   unsigned int *__restrict__ kmax2_bits)
+__global__ void __launch_bounds__(256) kmax_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                   const __nv_bfloat16 *__restrict__ k, int N, int nblk,
+                                                   unsigned int *__restrict__ kmax2_bits, float2 *__restrict__ rows)
 {
-    constexpr int LPK = D / 8, KPW = 32 / LPK;  // lanes per key, keys per warp pass
+    constexpr int LPK = D / 8, KPW = 32 / LPK;  // lanes per row, rows per warp pass
+    constexpr int kStep = 8 * KPW;              // rows per CTA pass (8 warps)
+    constexpr int kUnroll = 4;
     const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(nblk));
     const int blk = static_cast<int>(blockIdx.x - static_cast<unsigned>(bh) * nblk);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane / LPK, l = lane % LPK;
-    const __nv_bfloat16 *kb = k + static_cast<size_t>(bh) * N * D;
+    const size_t base = static_cast<size_t>(bh) * N * D;
+    const int end = min(N, (blk + 1) * kPlanRows);
     float best = 0.f;
-    for (int j0 = blk * 256 + warp * KPW; j0 < min(N, (blk + 1) * 256); j0 += 8 * KPW) {
-        const int j = j0 + sub;
-        float s = 0.f;
-        if (j < N) {
-            float f[8];
-            bf16x8(*reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(j) * D + 8 * l), f);
+    // the loop index is the same for every lane of the warp (the shuffles below need
+    // the whole warp); the lane's row is j0 + sub
+    for (int j0 = blk * kPlanRows + warp * KPW; j0 < end; j0 += kUnroll * kStep) {
+        uint4 uk[kUnroll], uq[kUnroll];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) s = fmaf(f[t], f[t], s);
+        for (int t = 0; t < kUnroll; ++t) {
+            const int j = j0 + sub + t * kStep;
+            if (j < end) {
+                uk[t] = *reinterpret_cast<const uint4 *>(k + base + static_cast<size_t>(j) * D + 8 * l);
+                uq[t] = *reinterpret_cast<const uint4 *>(q + base + static_cast<size_t>(j) * D + 8 * l);
+            }
         }
-        s = group_sum<LPK>(s);
-        best = fmaxf(best, s);
+#pragma unroll
+        for (int t = 0; t < kUnroll; ++t) {
+            const int j = j0 + sub + t * kStep;
+            float kk = 0.f, qq = 0.f, qk = 0.f;
+            if (j < end) {
+                float fk[8], fq[8];
+                bf16x8(uk[t], fk);
+                bf16x8(uq[t], fq);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    kk = fmaf(fk[e], fk[e], kk);
+                    qq = fmaf(fq[e], fq[e], qq);
+                    qk = fmaf(fq[e], fk[e], qk);
+                }
+            }
+            kk = group_sum<LPK>(kk);
+            qq = group_sum<LPK>(qq);
+            qk = group_sum<LPK>(qk);
+            if (j < end) {
+                best = fmaxf(best, kk);
+                if (l == 0) rows[static_cast<size_t>(bh) * N + j] = make_float2(qq, qk);
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
@@ -85,57 +116,39 @@ __global__ void __launch_bounds__(256) kmax_kernel(const __nv_bfloat16 *__restri
     }
 }
 
-// First KV tile worth computing per work item: one CTA per item, 256 threads,
-// LPK lanes per query row. info[w] = (first tile, tiles the item then spans).
-template <int D>
-__global__ void __launch_bounds__(256) item_plan_kernel(const __nv_bfloat16 *__restrict__ q,
-                                                        const __nv_bfloat16 *__restrict__ k,
-                                                        const unsigned int *__restrict__ kmax2_bits, int N, int H,
-                                                        int NQB, int NQT, float c1, Slopes slopes,
-                                                        int2 *__restrict__ info)
+// First KV tile worth computing per work item: one CTA per item, one thread per
+// query row (256). info[w] = (first tile, tiles the item then spans).
+__global__ void __launch_bounds__(kPlanRows) item_plan_kernel(const float2 *__restrict__ rows,
+                                                              const unsigned int *__restrict__ kmax2_bits, int N,
+                                                              int H, int NQB, int NQT, float c1, Slopes slopes,
+                                                              int2 *__restrict__ info)
 {
-    constexpr int LPK = D / 8, KPW = 32 / LPK;
     const int w = blockIdx.x;
     const int bh = w / NQB, qb = w - bh * NQB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane / LPK, l = lane % LPK;
-    const size_t base = static_cast<size_t>(bh) * N * D;
     // fp32 is ample here: the bound keeps a whole unit of exponent margin, and fp32
     // rounding moves the cut by ~1e-3 tokens (~1e-3 m log2(e) exponent units).
     const float kmax = sqrtf(__uint_as_float(kmax2_bits[bh]));
     const float sl2 = slopes.log2e[bh % H];
-    float cut = 3.0e38f;  // min over this thread's rows of i - D_i
-    for (int r0 = warp * KPW; r0 < kPlanRows; r0 += 8 * KPW) {
-        const int i = qb * kPlanRows + r0 + sub;
-        float qq = 0.f, qk = 0.f;
-        if (i < N) {
-            float fq[8], fk[8];
-            bf16x8(*reinterpret_cast<const uint4 *>(q + base + static_cast<size_t>(i) * D + 8 * l), fq);
-            bf16x8(*reinterpret_cast<const uint4 *>(k + base + static_cast<size_t>(i) * D + 8 * l), fk);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                qq = fmaf(fq[t], fq[t], qq);
-                qk = fmaf(fq[t], fk[t], qk);
-            }
-        }
-        qq = group_sum<LPK>(qq);
-        qk = group_sum<LPK>(qk);
-        if (i < N && l == 0) {
-            // 2^-10 relative slack on the norm product and on |q.k| absorbs the rounding of
-            // these sums and of the kernel's scores (both far below 2^-10 relative).
-            const float slack = 1.0f + 0x1p-10f;
-            const float a = c1 * (sqrtf(qq) * kmax * slack * slack - qk + fabsf(qk) * 0x1p-10f) + 127.0f;
-            cut = fminf(cut, static_cast<float>(i) - a / sl2);
-        }
+    float cut = 3.0e38f;  // min over the item's rows of i - D_i
+    const int i = qb * kPlanRows + static_cast<int>(threadIdx.x);
+    if (i < N) {
+        const float2 r = rows[static_cast<size_t>(bh) * N + i];
+        const float qq = r.x, qk = r.y;
+        // 2^-10 relative slack on the norm product and on |q.k| absorbs the rounding of
+        // these sums and of the kernel's scores (both far below 2^-10 relative).
+        const float slack = 1.0f + 0x1p-10f;
+        const float a = c1 * (sqrtf(qq) * kmax * slack * slack - qk + fabsf(qk) * 0x1p-10f) + 127.0f;
+        cut = static_cast<float>(i) - a / sl2;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) cut = fminf(cut, __shfl_xor_sync(0xffffffffu, cut, o));
-    __shared__ float red[8];
+    __shared__ float red[kPlanRows / 32];
     if (lane == 0) red[warp] = cut;
     __syncthreads();
     if (threadIdx.x == 0) {
         float m = red[0];
-        for (int ww = 1; ww < 8; ++ww) m = fminf(m, red[ww]);
+        for (int ww = 1; ww < kPlanRows / 32; ++ww) m = fminf(m, red[ww]);
         // tile jt (keys 128 jt .. 128 jt + 127) is skippable when 128 jt + 127 < m
         const int qt0 = 2 * qb, qt1 = 2 * qb + 1;
         const int n_nom = qt1 < NQT ? qt1 + 1 : qt1;
@@ -181,13 +194,22 @@ __global__ void plan_identity_kernel(const int2 *__restrict__ info, int items, i
 
 }  // namespace
 
-size_t skip_plan_bytes(int BH, int NQB)
+// Scratch of the plan: [plan | info | kmax2 | per-row sums], the last at a 256-byte
+// offset.
+static size_t rows_offset(int BH, int NQB)
 {
     const size_t items = static_cast<size_t>(BH) * NQB;
-    return 256 + items * 2 * sizeof(int2) + static_cast<size_t>(BH) * sizeof(unsigned int);
+    const size_t head = items * 2 * sizeof(int2) + static_cast<size_t>(BH) * sizeof(unsigned int);
+    return (head + 255) & ~static_cast<size_t>(255);
 }
 
-// Lays out [plan | info | kmax2] in `scratch` (skip_plan_bytes long) and fills it.
+size_t skip_plan_bytes(int BH, int N)
+{
+    const int NQB = ((N + 127) / 128 + 1) / 2;
+    return 256 + rows_offset(BH, NQB) + static_cast<size_t>(BH) * N * sizeof(float2);
+}
+
+// Lays out [plan | info | kmax2 | rows] in `scratch` (skip_plan_bytes long) and fills it.
 cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const Slopes &slopes,
                              void *scratch, int2 **plan_out, int2 **info_out, cudaStream_t stream)
 {
@@ -202,21 +224,18 @@ cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, 
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const int nblk = (N + 255) / 256;
     const unsigned g1 = static_cast<unsigned>(nblk) * static_cast<unsigned>(BH);  // <= 2^31 - 1 (check_dims)
-    if (d == 128) {
-        kmax_kernel<128><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
-        item_plan_kernel<128><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
-    } else if (d == 64) {
-        kmax_kernel<64><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
-        item_plan_kernel<64><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
-    } else if (d == 32) {
-        kmax_kernel<32><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
-        item_plan_kernel<32><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
-    } else if (d == 16) {
-        kmax_kernel<16><<<g1, 256, 0, stream>>>(kb, N, nblk, kmax2);
-        item_plan_kernel<16><<<items, 256, 0, stream>>>(qb, kb, kmax2, N, H, NQB, NQT, c1, slopes, info);
-    } else {
+    float2 *rows = reinterpret_cast<float2 *>(static_cast<uint8_t *>(scratch) + rows_offset(BH, NQB));
+    if (d == 128)
+        kmax_kernel<128><<<g1, 256, 0, stream>>>(qb, kb, N, nblk, kmax2, rows);
+    else if (d == 64)
+        kmax_kernel<64><<<g1, 256, 0, stream>>>(qb, kb, N, nblk, kmax2, rows);
+    else if (d == 32)
+        kmax_kernel<32><<<g1, 256, 0, stream>>>(qb, kb, N, nblk, kmax2, rows);
+    else if (d == 16)
+        kmax_kernel<16><<<g1, 256, 0, stream>>>(qb, kb, N, nblk, kmax2, rows);
+    else
         return cudaErrorInvalidValue;
-    }
+    item_plan_kernel<<<items, kPlanRows, 0, stream>>>(rows, kmax2, N, H, NQB, NQT, c1, slopes, info);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int max_len = NQT;  // no item spans more tiles than there are tiles
     // one int per bin within the 48 KB of dynamic shared memory a launch gets without

@@ -73,9 +73,9 @@ constexpr unsigned int kFwdLogDist = 4u;
 constexpr unsigned int kFwdSoftcap = 8u;
 constexpr unsigned int kFwdNominalOrder = 16u;
 
-// Underflow-skip plan (alibi_skip.cu): scratch size for B*H heads and NQB 256-row
-// blocks, and the launch that fills it ([plan | info | key norms]).
-size_t skip_plan_bytes(int BH, int NQB);
+// Underflow-skip plan (alibi_skip.cu): scratch size for B*H heads of N rows, and the
+// launch that fills it ([plan | info | key norms | per-row |q|^2 and q.k]).
+size_t skip_plan_bytes(int BH, int N);
 cudaError_t launch_skip_plan(const void *q, const void *k, int B, int H, int N, int d, const Slopes &slopes,
                              void *scratch, int2 **plan_out, int2 **info_out, cudaStream_t stream);
 

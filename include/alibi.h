@@ -124,8 +124,8 @@ typedef struct alibi_fwd_options {
  * every exponent in it is below -127 (base 2), where the kernel's
  * flush-to-zero exponential returns exactly 0. Output and LSE are therefore
  * bit-identical to the same call without the flag. The pre-pass reads Q and K
- * once and takes a small plan buffer (items x 16 bytes) from the library's
- * stream-ordered pool.
+ * once and takes a plan buffer (16 bytes per work item and 8 per query row)
+ * from the library's stream-ordered pool.
  *
  * ALIBI_FWD_CLAMP / _LOGDIST / _SOFTCAP: the mitigations of "When Attention
  * Goes Blind", sec. 3.4 (the paper trains with clamp_min = -87, sec. 4.3, and
