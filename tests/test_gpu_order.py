@@ -248,3 +248,40 @@ def test_backward_blocked_order_in_a_graph(ab):
         assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
         for a, b, name in zip(grads, g_ref, ("dq", "dk", "dv")):
             assert torch.equal(a, b), name
+
+
+CACHE_CHILD = r"""
+import torch
+import alibi_positional_bias_gb300 as ab
+ab.load()
+B, H, d = 4, 32, 128
+l2 = torch.cuda.get_device_properties(0).L2_cache_size
+g = torch.Generator(device="cuda").manual_seed(3)
+NMAX = 1100 + 4 * 263
+flat = [torch.randn(B * H * NMAX * d, device="cuda", generator=g).bfloat16() for _ in range(3)]
+checked = 0
+for t in range(264):
+    N = 1100 + 4 * t                  # 264 shapes, 5 to 9 blocks per head
+    assert 4 * B * H * N * d > l2 / 2
+    q, k, v = (f[: B * H * N * d].view(B, H, N, d) for f in flat)
+    o1, l1 = ab.alibi_attn_fwd(q, k, v)
+    if t in (0, 100, 255, 256, 263):  # before and past the 256 cached shapes
+        o2, l2_ = ab.alibi_attn_fwd_ex(q, k, v, flags=ab.ALIBI_FWD_NOMINAL_ORDER)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2_), t
+        checked += 1
+ab.alibi_check_error()
+print("ok", checked)
+"""
+
+
+def test_work_order_cache_full():
+    # more blocked-order shapes than the library caches tables for (256): the shapes
+    # past the cap keep the nominal order, with identical results and no error. A
+    # child process, so the full cache does not change the order other tests see.
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", CACHE_CHILD], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    assert r.stdout.strip().endswith("ok 5")
