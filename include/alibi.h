@@ -26,7 +26,8 @@
  *   - scale is 1/sqrt(d); slopes are always those of alibi_slopes(H).
  *   - The library keeps some state per device for the life of the process:
  *     the device status word, a stream-ordered memory pool, kernel attributes
- *     and the work-order tables of alibi_attn_fwd_ex. cudaDeviceReset() of a
+ *     and the work-order tables of the prefill and backward (see
+ *     alibi_attn_fwd_ex). cudaDeviceReset() of a
  *     device destroys that state with the context; do not call the library on
  *     that device again in the same process after a reset.
  *   - Return value: ALIBI_OK, or a negative alibi_status. Argument errors are
@@ -85,6 +86,8 @@ ALIBI_API int alibi_slopes(int H, float *out_host);
  * Runs the tcgen05/TMEM/TMA kernel: scores and P.V on the tensor cores with
  * fp32 accumulation; the bias is generated from tile coordinates and never
  * stored; online softmax in fp32; P rounded to bf16 for the P.V product.
+ * Large launches take the blocked work order described under
+ * alibi_attn_fwd_ex (same results).
  */
 ALIBI_API int alibi_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
                    int B, int H, int N, int d, int causal, void *stream);
