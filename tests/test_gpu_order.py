@@ -285,3 +285,33 @@ def test_work_order_cache_full():
     r = subprocess.run([sys.executable, "-c", CACHE_CHILD], cwd=root, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
     assert r.stdout.strip().endswith("ok 5")
+
+
+def test_blocked_order_random_shapes(ab):
+    # 16 seeded random launches above half the L2 (ragged N, every head size, either
+    # mask, plain or mitigated): forward and (d = 64 / 128) backward bit-identical to
+    # the nominal order
+    import random
+    import torch
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    rng = random.Random(2026)
+    done = 0
+    while done < 16:
+        d = rng.choice([16, 32, 64, 128])
+        B, H, N = rng.randint(1, 32), rng.randint(1, 64), rng.randint(300, 8192)
+        causal = rng.random() < 0.7
+        if 4 * B * H * N * d <= l2 / 2 or B * H * N * d > 2 ** 31:
+            continue
+        flags = rng.choice([0, 0, 0, ab.ALIBI_FWD_CLAMP, ab.ALIBI_FWD_LOGDIST, ab.ALIBI_FWD_SOFTCAP])
+        g = torch.Generator(device="cuda").manual_seed(done)
+        q, k, v, do = (torch.randn(B, H, N, d, device="cuda", generator=g).bfloat16() for _ in range(4))
+        kw = dict(causal=causal, clamp_min=-30.0, softcap_z=40.0)
+        o1, l1 = ab.alibi_attn_fwd_ex(q, k, v, flags=flags, **kw)
+        o2, l2_ = ab.alibi_attn_fwd_ex(q, k, v, flags=flags | ab.ALIBI_FWD_NOMINAL_ORDER, **kw)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2_), (B, H, N, d, causal, flags)
+        if d in (64, 128):
+            g1 = ab.alibi_attn_bwd(q, k, v, o1, l1, do, flags=flags, **kw)
+            g2 = ab.alibi_attn_bwd(q, k, v, o1, l1, do, flags=flags | ab.ALIBI_FWD_NOMINAL_ORDER, **kw)
+            assert all(torch.equal(a, b) for a, b in zip(g1, g2)), (B, H, N, d, causal, flags)
+        ab.alibi_check_error()
+        done += 1
